@@ -1,0 +1,201 @@
+/*
+ * ring_attn.h -- C ABI of libringattn.so: blockwise ring attention on one
+ * NVIDIA B300 (sm_103a).
+ *
+ * What is computed.  Ring attention ("Sequenzparallelitaet und
+ * Ringaufmerksamkeit", section "Tiefer Einblick"; "Context parallelism and
+ * zig-zag ring attention", section "Zig Zag Ring Attention") splits a
+ * sequence of S tokens into P shards.  Each shard keeps its queries while the
+ * key/value blocks of all shards travel around a ring; at ring step t shard r
+ * holds the block of shard s = (r - t) mod P, computes partial attention and
+ * folds it into a running maximum and normaliser (online softmax), rescaling
+ * the earlier partial sums.  After P steps every query has attended to every
+ * key, and the result equals full attention.  On one GPU the P ring ranks are
+ * virtual shards: the ring is a block schedule, no bytes cross a GPU boundary.
+ *
+ * Shard layouts (which tokens a shard owns; n = S / P, C = S / (2P)):
+ *   RA_LAYOUT_CONTIGUOUS  shard r owns tokens [r*n, (r+1)*n)  ("Tiefer Einblick").
+ *   RA_LAYOUT_STRIPED     token i belongs to shard i mod P  (the interleaving
+ *                         shown in "Zig Zag Ring Attention": GPU 0 gets tokens
+ *                         0, 4, 8, ..., GPU 1 gets 1, 5, 9, ...; that page
+ *                         calls it zig-zag).
+ *   RA_LAYOUT_ZIGZAG      cut into 2P chunks of C tokens; shard r owns chunks r
+ *                         and 2P-1-r (the variant named in "Die Zukunft der
+ *                         Sequenzparallelitaet"; the pages give no definition,
+ *                         this is the reading this library implements).
+ * Inside a shard, tokens keep increasing global position ("local slot" j).
+ * The causal mask always compares GLOBAL positions: query i sees key j iff
+ * j <= i ("Zig Zag Ring Attention": an autoregressive token only sees earlier
+ * tokens).
+ *
+ * Tensors (row-major, caller-allocated, device memory unless stated):
+ *   q, out, dout, dq   [B][S][H][D]    natural token order
+ *   k, v, dk, dv       [B][S][Hkv][D]  natural token order
+ *   lse                [B][H][S]       fp32, natural log-sum-exp of the scaled
+ *                                      scores (lse = m + ln l)
+ *   q_shard, out_part  [B][n][H][D]    one shard, local-slot order
+ *   k_shard, v_shard   [B][n][Hkv][D]  one shard, local-slot order
+ *   lse_part           [B][H][n]       fp32
+ * bf16 unless stated.  Query head h reads key/value head h / (H / Hkv).
+ * D must be 64 or 128.  Every pointer must be 16-byte aligned.
+ *
+ * Ownership and ordering.  The caller owns every buffer; the library keeps no
+ * pointer after a call returns.  Every call is asynchronous and ordered on
+ * `stream` (a cudaStream_t passed as void*, NULL = legacy default stream).
+ * Transient workspace, when a call needs one, is taken with cudaMallocAsync
+ * and released with cudaFreeAsync on that stream.  Calls on different streams
+ * may run concurrently.
+ *
+ * Errors.  Argument errors are detected on the host before anything is
+ * launched and return a nonzero ra_status; ring_attn_last_error() then gives
+ * a message (per host thread).  A failed launch returns RA_ERR_CUDA.  Kernel
+ * waits are bounded in time: a pipeline that stops making progress gives up
+ * after about two seconds and leaves a code that ring_attn_check_status()
+ * reports as RA_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef RING_ATTN_H
+#define RING_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_NULL = 1,           /* a required pointer is NULL */
+  RA_ERR_SHAPE = 2,          /* sizes inconsistent or out of range */
+  RA_ERR_LAYOUT = 3,         /* unknown layout, or S not divisible as it needs */
+  RA_ERR_UNSUPPORTED = 4,    /* D not 64/128, non-finite scale, no sm_100-class GPU */
+  RA_ERR_ALIGN = 5,          /* a pointer is not 16-byte aligned */
+  RA_ERR_CUDA = 6,           /* a CUDA runtime call or launch failed */
+  RA_ERR_DEVICE_TIMEOUT = 7, /* a kernel gave up waiting (see ring_attn_check_status) */
+  RA_ERR_ALLOC = 8           /* workspace allocation failed */
+} ra_status;
+
+typedef enum {
+  RA_LAYOUT_CONTIGUOUS = 0,
+  RA_LAYOUT_STRIPED = 1,
+  RA_LAYOUT_ZIGZAG = 2
+} ra_layout;
+
+typedef enum { RA_BF16 = 0, RA_F32 = 1 } ra_dtype;
+
+/*
+ * ring_attn_fwd -- the whole ring: for every shard r, steps t = 0..P-1 over
+ * blocks s = (r - t) mod P, online-softmax accumulation, final normalisation.
+ * ("Tiefer Einblick": after one full loop every query has attended to every
+ * key.)  Equal to softmax(scale * q k^T + causal mask) v.
+ *   out:  [B][S][H][D], bf16 (out_dtype RA_BF16) or fp32 (RA_F32).
+ *   lse:  [B][H][S] fp32 (may be NULL if not wanted).
+ *   scale: multiplies q.k before the softmax (usually 1/sqrt(D)); finite.
+ * Needs S % P == 0 (and S % 2P == 0 for zig-zag), H % Hkv == 0, S >= 1.
+ * Key blocks that the causal mask hides entirely are skipped, never computed.
+ */
+ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out,
+                        ra_dtype out_dtype, float* lse, int B, int H, int Hkv, int64_t S,
+                        int D, int P, ra_layout layout, int causal, float scale,
+                        void* stream);
+
+/*
+ * ring_attn_fwd_counted -- ring_attn_fwd that also adds, for each shard r, the
+ * number of (128-query tile, 128-key tile) blocks the kernel actually
+ * multiplied into shard_tiles[r] (device, int64[P], caller-zeroed).  The
+ * per-shard totals measure the causal load balance the interleaved layouts are
+ * meant to fix ("Zig Zag Ring Attention": with contiguous shards the later
+ * ranks carry more work and the earlier ones idle).
+ */
+ra_status ring_attn_fwd_counted(const void* q, const void* k, const void* v, void* out,
+                                ra_dtype out_dtype, float* lse, int B, int H, int Hkv,
+                                int64_t S, int D, int P, ra_layout layout, int causal,
+                                float scale, int64_t* shard_tiles, void* stream);
+
+/*
+ * ring_attn_bwd -- gradients of ring_attn_fwd (the pages describe the forward
+ * only; this is the standard softmax-attention gradient):
+ *   P = exp(scale q k^T - lse), delta = rowsum(dout * out),
+ *   dv = P^T dout, dS = P * (dout v^T - delta), dq = scale dS k, dk = scale dS^T q,
+ * with dk, dv summed over the H/Hkv query heads sharing a key/value head.
+ *   out, lse: the forward's outputs (out bf16).  dq, dk, dv: bf16 outputs.
+ * Uses an fp32 workspace of B*S*H*D*4 + B*H*S*4 bytes (cudaMallocAsync).
+ */
+ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                        int B, int H, int Hkv, int64_t S, int D, int P, ra_layout layout,
+                        int causal, float scale, void* stream);
+
+/*
+ * ring_attn_step -- one ring hop: the queries of shard r against the key/value
+ * block of shard s only ("Tiefer Einblick": as each block arrives the GPU
+ * computes a partial attention), causal on global positions, normalised
+ * within the block.
+ *   q_shard [B][n][H][D], k_shard/v_shard [B][n][Hkv][D] (bf16, local order);
+ *   out_part [B][n][H][D] fp32, lse_part [B][H][n] fp32.
+ * A query that sees no key of the block gets out_part 0 and lse_part -inf.
+ */
+ra_status ring_attn_step(const void* q_shard, const void* k_shard, const void* v_shard,
+                         float* out_part, float* lse_part, int B, int H, int Hkv, int64_t S,
+                         int D, int P, ra_layout layout, int r, int s, int causal, float scale,
+                         void* stream);
+
+/*
+ * ring_attn_merge -- fold one partial into a running result, the online
+ * softmax accumulation across hops ("Tiefer Einblick"; "technical insight"
+ * of the Thai edition: keep a running maximum and normaliser and rescale the
+ * earlier partial sums).  With lse = ln(e^lse_acc + e^lse_part):
+ *   out_acc = e^(lse_acc - lse) out_acc + e^(lse_part - lse) out_part,
+ *   lse_acc = lse.
+ * out_* [B][n][H][D] fp32, lse_* [B][H][n] fp32; in place on (out_acc, lse_acc).
+ * A -inf lse on one side leaves the other unchanged; both -inf gives (0, -inf).
+ */
+ra_status ring_attn_merge(float* out_acc, float* lse_acc, const float* out_part,
+                          const float* lse_part, int B, int H, int64_t n, int D, void* stream);
+
+/*
+ * ring_attn_permute -- move token rows between natural order and shard-major
+ * order: dst[o][r*n + j] = src[o][pos_r(j)] (inverse = 0), or the reverse
+ * scatter (inverse != 0), for o < outer, where pos_r(j) is the global position
+ * held in local slot j of shard r under `layout`.  row_bytes is the size of
+ * one token row (H*D*2 for a bf16 [B][S][H][D] tensor with outer = B; 4 for an
+ * lse tensor with outer = B*H) and must be a multiple of 4.  src and dst must
+ * not overlap.
+ */
+ra_status ring_attn_permute(const void* src, void* dst, int64_t outer, int64_t S,
+                            int64_t row_bytes, int P, ra_layout layout, int inverse,
+                            void* stream);
+
+/*
+ * ring_attn_index_map -- host-side layout map: pos[r*n + j] = global position
+ * of local slot j of shard r (host array of S int64).  No GPU involved.
+ */
+ra_status ring_attn_index_map(int64_t S, int P, ra_layout layout, int64_t* pos);
+
+/*
+ * ring_attn_census -- host-side per-shard work accounting under the kernels'
+ * tiling (128-slot tiles that never straddle a contiguous run of positions):
+ * visible_pairs[r] = number of (query, key) pairs the mask lets shard r's
+ * queries see; computed_tiles[r] = number of (query tile, key tile) blocks
+ * the forward kernel multiplies for shard r.  Either pointer may be NULL.
+ */
+ra_status ring_attn_census(int64_t S, int P, ra_layout layout, int causal,
+                           int64_t* visible_pairs, int64_t* computed_tiles);
+
+/*
+ * ring_attn_check_status -- waits for `stream`, then reports and clears the
+ * device status word: RA_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded
+ * wait since the last check, RA_ERR_CUDA if the stream holds an error, else RA_OK.
+ */
+ra_status ring_attn_check_status(void* stream);
+
+/* ring_attn_last_error -- message for the last failing call on this host thread. */
+const char* ring_attn_last_error(void);
+
+/* ring_attn_version -- library version string. */
+const char* ring_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RING_ATTN_H */

@@ -124,6 +124,24 @@ def attn_fwd(q, k, v, causal: bool, scale: float, rows=None, nthreads=None):
     return out, lse
 
 
+def attn_fwd_rows(qrows, rows, k, v, causal: bool, scale: float, nthreads=None):
+    """Like attn_fwd for the queries at positions ``rows`` only, given just
+    those query rows: qrows [B, len(rows), H, D]; k/v [B, S, Hkv, D]."""
+    qrows = _f64(qrows)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    k, v = _f64(k), _f64(v)
+    B, nr, H, D = qrows.shape
+    S, Hkv = k.shape[1], k.shape[2]
+    out = np.empty((B, nr, H, D))
+    lse = np.empty((B, H, nr))
+    rc = _load().oracle_attn_fwd_rows(_ptr(qrows), _ptr(k), _ptr(v), B, H, Hkv, S, D,
+                                      int(bool(causal)), float(scale), _ptr(rows), nr,
+                                      _ptr(out), _ptr(lse), _threads(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd_rows: bad arguments")
+    return out, lse
+
+
 def ring_fwd(q, k, v, P: int, layout, causal: bool, scale: float, nthreads=None):
     """Ring-order blockwise attention with online softmax (fp64, natural order)."""
     q, k, v = _f64(q), _f64(k), _f64(v)

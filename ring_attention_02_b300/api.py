@@ -1,0 +1,206 @@
+"""Python binding of libringattn.so (ctypes).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI of ``include/ring_attn.h``.  torch supplies device
+memory and streams.  If the shared library is missing the first call raises:
+there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libringattn.so")
+
+LAYOUTS = {"contiguous": 0, "striped": 1, "zigzag": 2}
+RA_BF16, RA_F32 = 0, 1
+STATUS = {0: "RA_OK", 1: "RA_ERR_NULL", 2: "RA_ERR_SHAPE", 3: "RA_ERR_LAYOUT",
+          4: "RA_ERR_UNSUPPORTED", 5: "RA_ERR_ALIGN", 6: "RA_ERR_CUDA",
+          7: "RA_ERR_DEVICE_TIMEOUT", 8: "RA_ERR_ALLOC"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} not built; run __graft_entry__.build() "
+                                   "or python ring_attention_02_b300/build.py")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+            L.ring_attn_fwd.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i64, i32, i32,
+                                        i32, i32, f32, vp]
+            L.ring_attn_fwd_counted.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i64, i32,
+                                                i32, i32, i32, f32, vp, vp]
+            L.ring_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64,
+                                        i32, i32, i32, i32, f32, vp]
+            L.ring_attn_step.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, i32, i32,
+                                         i32, i32, i32, f32, vp]
+            L.ring_attn_merge.argtypes = [vp, vp, vp, vp, i32, i32, i64, i32, vp]
+            L.ring_attn_permute.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, vp]
+            L.ring_attn_index_map.argtypes = [i64, i32, i32, vp]
+            L.ring_attn_census.argtypes = [i64, i32, i32, i32, vp, vp]
+            L.ring_attn_check_status.argtypes = [vp]
+            L.ring_attn_last_error.restype = ctypes.c_char_p
+            L.ring_attn_version.restype = ctypes.c_char_p
+            for name in ("ring_attn_fwd", "ring_attn_fwd_counted", "ring_attn_bwd",
+                         "ring_attn_step", "ring_attn_merge", "ring_attn_permute",
+                         "ring_attn_index_map", "ring_attn_census", "ring_attn_check_status"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+        return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise RingAttnError(status, lib().ring_attn_last_error().decode())
+
+
+def _layout(layout) -> int:
+    return LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def fwd(q, k, v, P: int, layout, causal: bool = True, scale: float | None = None,
+        out_dtype=torch.bfloat16, out=None, lse=None, want_lse: bool = True, stream=None):
+    """Ring attention forward.  q [B,S,H,D], k/v [B,S,Hkv,D] bf16 (natural order).
+
+    Returns (out [B,S,H,D] in out_dtype, lse [B,H,S] fp32 or None).
+    """
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, nm)
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=out_dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    odt = RA_F32 if out.dtype == torch.float32 else RA_BF16
+    _check(lib().ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), odt, _ptr(lse), B, H, Hkv,
+                               S, D, P, _layout(layout), int(bool(causal)), float(scale),
+                               _stream(stream)))
+    return out, lse
+
+
+def fwd_counted(q, k, v, P: int, layout, causal: bool = True, scale: float | None = None,
+                out_dtype=torch.bfloat16, stream=None):
+    """fwd plus the per-shard count of multiplied (query tile, key tile) blocks,
+    summed over batch and heads."""
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = D ** -0.5
+    out = torch.empty((B, S, H, D), dtype=out_dtype, device=q.device)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    tiles = torch.zeros(P, dtype=torch.int64, device=q.device)
+    odt = RA_F32 if out_dtype == torch.float32 else RA_BF16
+    _check(lib().ring_attn_fwd_counted(_ptr(q), _ptr(k), _ptr(v), _ptr(out), odt, _ptr(lse), B,
+                                       H, Hkv, S, D, P, _layout(layout), int(bool(causal)),
+                                       float(scale), _ptr(tiles), _stream(stream)))
+    return out, lse, tiles
+
+
+def bwd(q, k, v, out, lse, dout, P: int, layout, causal: bool = True,
+        scale: float | None = None, stream=None):
+    """Gradients (dq, dk, dv), bf16, natural order."""
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = D ** -0.5
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    _check(lib().ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, P,
+                               _layout(layout), int(bool(causal)), float(scale),
+                               _stream(stream)))
+    return dq, dk, dv
+
+
+def step(q_shard, k_shard, v_shard, S: int, P: int, layout, r: int, s: int,
+         causal: bool = True, scale: float | None = None, stream=None):
+    """One ring hop in shard-local order: (out_part fp32 [B,n,H,D], lse_part [B,H,n])."""
+    B, n, H, D = q_shard.shape
+    Hkv = k_shard.shape[2]
+    if scale is None:
+        scale = D ** -0.5
+    out = torch.empty((B, n, H, D), dtype=torch.float32, device=q_shard.device)
+    lse = torch.empty((B, H, n), dtype=torch.float32, device=q_shard.device)
+    _check(lib().ring_attn_step(_ptr(q_shard), _ptr(k_shard), _ptr(v_shard), _ptr(out),
+                                _ptr(lse), B, H, Hkv, S, D, P, _layout(layout), r, s,
+                                int(bool(causal)), float(scale), _stream(stream)))
+    return out, lse
+
+
+def merge(out_acc, lse_acc, out_part, lse_part, stream=None):
+    """In-place LSE fold of (out_part, lse_part) into (out_acc, lse_acc)."""
+    B, n, H, D = out_acc.shape
+    _check(lib().ring_attn_merge(_ptr(out_acc), _ptr(lse_acc), _ptr(out_part), _ptr(lse_part),
+                                 B, H, n, D, _stream(stream)))
+    return out_acc, lse_acc
+
+
+def permute(src, S: int, P: int, layout, inverse: bool = False, out=None, stream=None):
+    """Rows of src [outer, S, ...] to shard-major order (or back, inverse=True)."""
+    outer = src.shape[0]
+    row_bytes = src.numel() * src.element_size() // (outer * S)
+    dst = torch.empty_like(src) if out is None else out
+    _check(lib().ring_attn_permute(_ptr(src), _ptr(dst), outer, S, row_bytes, P,
+                                   _layout(layout), int(bool(inverse)), _stream(stream)))
+    return dst
+
+
+def index_map(S: int, P: int, layout):
+    """Host-side map, torch int64 [P, S//P] of global positions."""
+    pos = torch.empty(S, dtype=torch.int64)
+    _check(lib().ring_attn_index_map(S, P, _layout(layout), ctypes.c_void_p(pos.data_ptr())))
+    return pos.view(P, S // P)
+
+
+def census(S: int, P: int, layout, causal: bool = True):
+    """Host-side per-shard (visible pairs, computed 128x128 tiles) for one (b, h)."""
+    pairs = torch.empty(P, dtype=torch.int64)
+    tiles = torch.empty(P, dtype=torch.int64)
+    _check(lib().ring_attn_census(S, P, _layout(layout), int(bool(causal)),
+                                  ctypes.c_void_p(pairs.data_ptr()),
+                                  ctypes.c_void_p(tiles.data_ptr())))
+    return pairs, tiles
+
+
+def check_status(stream=None):
+    """Synchronises the stream and raises if a kernel reported a timeout."""
+    _check(lib().ring_attn_check_status(_stream(stream)))
+
+
+def version() -> str:
+    return lib().ring_attn_version().decode()

@@ -1,0 +1,371 @@
+// ring_attn.cu -- libringattn.so: the C ABI declared in include/ring_attn.h.
+// Host side: argument checks, TMA tensor maps, launch shapes.  The library is
+// one translation unit; the kernels live in the included headers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/ring_attn.h"
+#include "attn_fwd.cuh"
+#include "elementwise.cuh"
+#include "geometry.cuh"
+#include "sm103_ptx.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+ra_status fail(ra_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+ra_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(RA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- device facts
+struct DeviceInfo {
+  int sms = 0;
+  int cc_major = 0;
+  bool fwd_attr_set[2] = {false, false};
+  bool bwd_attr_set[2] = {false, false};
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+ra_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(RA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.sms == 0) {
+    int sms = 0, major = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(CC)");
+    d.sms = sms;
+    d.cc_major = major;
+  }
+  if (d.cc_major != 10)
+    return fail(RA_ERR_UNSUPPORTED, "needs a Blackwell sm_10x GPU (found compute capability %d.x)",
+                d.cc_major);
+  *out = &d;
+  return RA_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+ra_status encode_fn(EncodeTiledFn* fn) {
+  static EncodeTiledFn cached = nullptr;
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                           &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) cached = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (cached == nullptr) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  *fn = cached;
+  return RA_OK;
+}
+
+// 4-d bf16 view {D, heads, phases, rows} of a token tensor whose row `R` at
+// phase `ph` starts at base + (R * phases + ph) * heads * D * 2 bytes.
+// Box {64, 1, 1, 128}, 128-byte swizzle (the layout tcgen05 descriptors use).
+ra_status make_token_map(CUtensorMap* m, const void* base, int D, int heads, int64_t phases,
+                         int64_t rows) {
+  EncodeTiledFn fn = nullptr;
+  ra_status st = encode_fn(&fn);
+  if (st != RA_OK) return st;
+  const cuuint64_t row_bytes = (cuuint64_t)heads * D * 2;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)phases, (cuuint64_t)rows};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, row_bytes, row_bytes * (cuuint64_t)phases};
+  cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)ra::kTile};
+  cuuint32_t elem[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return RA_OK;
+}
+
+// ---------------------------------------------------------------- checks
+ra_status check_common(int B, int H, int Hkv, int64_t S, int D, int P, int layout, float scale) {
+  if (B < 1 || H < 1 || Hkv < 1 || S < 1 || P < 1)
+    return fail(RA_ERR_SHAPE, "sizes must be positive (B=%d H=%d Hkv=%d S=%lld P=%d)", B, H, Hkv,
+                (long long)S, P);
+  if (H % Hkv != 0) return fail(RA_ERR_SHAPE, "H=%d is not a multiple of Hkv=%d", H, Hkv);
+  if (D != 64 && D != 128) return fail(RA_ERR_UNSUPPORTED, "head dim D=%d (supported: 64, 128)", D);
+  if (layout < 0 || layout > 2) return fail(RA_ERR_LAYOUT, "unknown layout %d", layout);
+  if (S % P != 0) return fail(RA_ERR_LAYOUT, "S=%lld is not divisible by P=%d", (long long)S, P);
+  if (layout == RA_LAYOUT_ZIGZAG && S % (2 * (int64_t)P) != 0)
+    return fail(RA_ERR_LAYOUT, "zig-zag needs S=%lld divisible by 2P=%d", (long long)S, 2 * P);
+  if (!std::isfinite(scale)) return fail(RA_ERR_UNSUPPORTED, "scale is not finite");
+  if ((int64_t)B * S > 0x7fffffffLL)
+    return fail(RA_ERR_SHAPE, "B*S=%lld exceeds the 2^31 rows a tensor map addresses",
+                (long long)((int64_t)B * S));
+  return RA_OK;
+}
+
+template <int D>
+ra_status launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const ra::FwdParams& prm, DeviceInfo* dev, cudaStream_t stream) {
+  const size_t smem = sizeof(ra::FwdSmem<D>) + 1024;
+  const int di = D == 128 ? 1 : 0;
+  if (!dev->fwd_attr_set[di]) {
+    cudaError_t e = cudaFuncSetAttribute(ra::attn_fwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd smem)");
+    dev->fwd_attr_set[di] = true;
+  }
+  if (prm.num_items == 0) return RA_OK;
+  const int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  ra::attn_fwd_kernel<D><<<(unsigned)grid, 384, smem, stream>>>(mq, mk, mv, prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel launch");
+  return RA_OK;
+}
+
+ra_status fwd_impl(int mode, const void* q, const void* k, const void* v, void* out, int out_f32,
+                   float* lse, int B, int H, int Hkv, int64_t S, int D, int P, int layout,
+                   int causal, float scale, int r, int s, unsigned long long* shard_tiles,
+                   cudaStream_t stream) {
+  if (!q || !k || !v || !out) return fail(RA_ERR_NULL, "q, k, v and out must be non-NULL");
+  ra_status st = check_common(B, H, Hkv, S, D, P, layout, scale);
+  if (st != RA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(RA_ERR_ALIGN, "q, k, v and out must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(RA_ERR_ALIGN, "lse must be 4-byte aligned");
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != RA_OK) return st;
+
+  ra::FwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.g = ra::make_geo(B, H, Hkv, S, P, layout, causal ? 1 : 0);
+  prm.mode = mode;
+  prm.step_r = r;
+  prm.step_s = s;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.out = out;
+  prm.out_f32 = out_f32;
+  prm.lse = lse;
+  prm.shard_tiles = shard_tiles;
+  const bool step = mode == ra::FWD_MODE_STEP;
+  prm.num_items = ra::units_total(prm.g, step) * B * H;
+
+  CUtensorMap mq, mk, mv;
+  const int64_t n = S / P;
+  if (step) {
+    st = make_token_map(&mq, q, D, H, 1, (int64_t)B * n);
+    if (st == RA_OK) st = make_token_map(&mk, k, D, Hkv, 1, (int64_t)B * n);
+    if (st == RA_OK) st = make_token_map(&mv, v, D, Hkv, 1, (int64_t)B * n);
+  } else if (layout == RA_LAYOUT_STRIPED) {
+    st = make_token_map(&mq, q, D, H, P, (int64_t)B * n);
+    if (st == RA_OK) st = make_token_map(&mk, k, D, Hkv, P, (int64_t)B * n);
+    if (st == RA_OK) st = make_token_map(&mv, v, D, Hkv, P, (int64_t)B * n);
+  } else {
+    st = make_token_map(&mq, q, D, H, 1, (int64_t)B * S);
+    if (st == RA_OK) st = make_token_map(&mk, k, D, Hkv, 1, (int64_t)B * S);
+    if (st == RA_OK) st = make_token_map(&mv, v, D, Hkv, 1, (int64_t)B * S);
+  }
+  if (st != RA_OK) return st;
+  return D == 128 ? launch_fwd_d<128>(mq, mk, mv, prm, dev, stream)
+                  : launch_fwd_d<64>(mq, mk, mv, prm, dev, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out, ra_dtype out_dtype,
+                        float* lse, int B, int H, int Hkv, int64_t S, int D, int P,
+                        ra_layout layout, int causal, float scale, void* stream) {
+  if (out_dtype != RA_BF16 && out_dtype != RA_F32)
+    return fail(RA_ERR_UNSUPPORTED, "out_dtype %d", (int)out_dtype);
+  return fwd_impl(ra::FWD_MODE_RING, q, k, v, out, out_dtype == RA_F32, lse, B, H, Hkv, S, D, P,
+                  layout, causal, scale, 0, 0, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_fwd_counted(const void* q, const void* k, const void* v, void* out,
+                                ra_dtype out_dtype, float* lse, int B, int H, int Hkv, int64_t S,
+                                int D, int P, ra_layout layout, int causal, float scale,
+                                int64_t* shard_tiles, void* stream) {
+  if (out_dtype != RA_BF16 && out_dtype != RA_F32)
+    return fail(RA_ERR_UNSUPPORTED, "out_dtype %d", (int)out_dtype);
+  if (!shard_tiles) return fail(RA_ERR_NULL, "shard_tiles must be non-NULL");
+  if (reinterpret_cast<uintptr_t>(shard_tiles) & 7u)
+    return fail(RA_ERR_ALIGN, "shard_tiles must be 8-byte aligned");
+  return fwd_impl(ra::FWD_MODE_RING, q, k, v, out, out_dtype == RA_F32, lse, B, H, Hkv, S, D, P,
+                  layout, causal, scale, 0, 0,
+                  reinterpret_cast<unsigned long long*>(shard_tiles),
+                  static_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                        int H, int Hkv, int64_t S, int D, int P, ra_layout layout, int causal,
+                        float scale, void* stream) {
+  (void)q; (void)k; (void)v; (void)out; (void)lse; (void)dout; (void)dq; (void)dk; (void)dv;
+  (void)B; (void)H; (void)Hkv; (void)S; (void)D; (void)P; (void)layout; (void)causal;
+  (void)scale; (void)stream;
+  return fail(RA_ERR_UNSUPPORTED, "backward kernels are not built into this library yet");
+}
+
+ra_status ring_attn_step(const void* q_shard, const void* k_shard, const void* v_shard,
+                         float* out_part, float* lse_part, int B, int H, int Hkv, int64_t S, int D,
+                         int P, ra_layout layout, int r, int s, int causal, float scale,
+                         void* stream) {
+  if (!lse_part) return fail(RA_ERR_NULL, "lse_part must be non-NULL");
+  if (P >= 1 && (r < 0 || r >= P || s < 0 || s >= P))
+    return fail(RA_ERR_SHAPE, "shard indices r=%d s=%d outside [0, %d)", r, s, P);
+  return fwd_impl(ra::FWD_MODE_STEP, q_shard, k_shard, v_shard, out_part, 1, lse_part, B, H, Hkv,
+                  S, D, P, layout, causal, scale, r, s, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_merge(float* out_acc, float* lse_acc, const float* out_part,
+                          const float* lse_part, int B, int H, int64_t n, int D, void* stream) {
+  if (!out_acc || !lse_acc || !out_part || !lse_part)
+    return fail(RA_ERR_NULL, "merge pointers must be non-NULL");
+  if (B < 1 || H < 1 || n < 1) return fail(RA_ERR_SHAPE, "sizes must be positive");
+  if (D != 64 && D != 128) return fail(RA_ERR_UNSUPPORTED, "head dim D=%d (supported: 64, 128)", D);
+  if (!aligned16(out_acc) || !aligned16(out_part))
+    return fail(RA_ERR_ALIGN, "out_acc and out_part must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse_acc) | reinterpret_cast<uintptr_t>(lse_part)) & 3u)
+    return fail(RA_ERR_ALIGN, "lse pointers must be 4-byte aligned");
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  const int64_t rows = (int64_t)B * n * H;
+  const int rows_per_block = 8 * (32 / (D / 4));
+  int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+  const int64_t cap = (int64_t)dev->sms * 8;
+  if (blocks > cap) blocks = cap;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (D == 128)
+    ra::merge_kernel<128><<<(unsigned)blocks, 256, 0, cs>>>(out_acc, lse_acc, out_part, lse_part, B, H, n);
+  else
+    ra::merge_kernel<64><<<(unsigned)blocks, 256, 0, cs>>>(out_acc, lse_acc, out_part, lse_part, B, H, n);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "merge_kernel launch");
+  return RA_OK;
+}
+
+ra_status ring_attn_permute(const void* src, void* dst, int64_t outer, int64_t S, int64_t row_bytes,
+                            int P, ra_layout layout, int inverse, void* stream) {
+  if (!src || !dst) return fail(RA_ERR_NULL, "src and dst must be non-NULL");
+  if (outer < 1 || S < 1 || P < 1 || row_bytes < 4 || row_bytes % 4 != 0)
+    return fail(RA_ERR_SHAPE, "bad permute sizes (outer=%lld S=%lld row_bytes=%lld P=%d)",
+                (long long)outer, (long long)S, (long long)row_bytes, P);
+  if ((int)layout < 0 || (int)layout > 2) return fail(RA_ERR_LAYOUT, "unknown layout %d", (int)layout);
+  if (S % P != 0) return fail(RA_ERR_LAYOUT, "S=%lld is not divisible by P=%d", (long long)S, P);
+  if (layout == RA_LAYOUT_ZIGZAG && S % (2 * (int64_t)P) != 0)
+    return fail(RA_ERR_LAYOUT, "zig-zag needs S divisible by 2P");
+  const uintptr_t a = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
+  if (a & 3u) return fail(RA_ERR_ALIGN, "src and dst must be 4-byte aligned");
+  const char* s8 = static_cast<const char*>(src);
+  const char* d8 = static_cast<const char*>(dst);
+  const int64_t bytes = outer * S * row_bytes;
+  if (s8 < d8 + bytes && d8 < s8 + bytes) return fail(RA_ERR_SHAPE, "src and dst overlap");
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  ra::Geo g = ra::make_geo(1, 1, 1, S, P, layout, 0);
+  const bool v16 = (a & 15u) == 0 && row_bytes % 16 == 0;
+  const int64_t pieces = outer * S * (row_bytes / (v16 ? 16 : 4));
+  int64_t blocks = (pieces + 255) / 256;
+  const int64_t cap = (int64_t)dev->sms * 16;
+  if (blocks > cap) blocks = cap;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (v16)
+    ra::permute_kernel<uint4><<<(unsigned)blocks, 256, 0, cs>>>(
+        static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), outer, g, row_bytes, inverse);
+  else
+    ra::permute_kernel<uint32_t><<<(unsigned)blocks, 256, 0, cs>>>(
+        static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), outer, g, row_bytes, inverse);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "permute_kernel launch");
+  return RA_OK;
+}
+
+ra_status ring_attn_index_map(int64_t S, int P, ra_layout layout, int64_t* pos) {
+  if (!pos) return fail(RA_ERR_NULL, "pos must be non-NULL");
+  if (S < 1 || P < 1) return fail(RA_ERR_SHAPE, "S and P must be positive");
+  if ((int)layout < 0 || (int)layout > 2) return fail(RA_ERR_LAYOUT, "unknown layout %d", (int)layout);
+  if (S % P != 0) return fail(RA_ERR_LAYOUT, "S is not divisible by P");
+  if (layout == RA_LAYOUT_ZIGZAG && S % (2 * (int64_t)P) != 0)
+    return fail(RA_ERR_LAYOUT, "zig-zag needs S divisible by 2P");
+  ra::Geo g = ra::make_geo(1, 1, 1, S, P, layout, 0);
+  for (int r = 0; r < P; ++r)
+    for (int64_t j = 0; j < g.n; ++j) pos[r * g.n + j] = ra::position_of(g, r, j);
+  return RA_OK;
+}
+
+ra_status ring_attn_census(int64_t S, int P, ra_layout layout, int causal, int64_t* visible_pairs,
+                           int64_t* computed_tiles) {
+  if (S < 1 || P < 1) return fail(RA_ERR_SHAPE, "S and P must be positive");
+  if ((int)layout < 0 || (int)layout > 2) return fail(RA_ERR_LAYOUT, "unknown layout %d", (int)layout);
+  if (S % P != 0) return fail(RA_ERR_LAYOUT, "S is not divisible by P");
+  if (layout == RA_LAYOUT_ZIGZAG && S % (2 * (int64_t)P) != 0)
+    return fail(RA_ERR_LAYOUT, "zig-zag needs S divisible by 2P");
+  ra::Geo g = ra::make_geo(1, 1, 1, S, P, layout, causal ? 1 : 0);
+  for (int r = 0; r < P; ++r) {
+    int64_t pairs = 0, tiles = 0;
+    for (int sq = 0; sq < g.nseg; ++sq) {
+      ra::Seg qs = ra::segment_of(g, r, sq);
+      for (int a = 0; a < g.ntile; ++a) {
+        ra::QTile qt = ra::make_qtile(g, r, sq, a);
+        if (!qt.valid) continue;
+        tiles += ra::tile_work(g, qt, -1);
+        // a query at position x sees keys 0..x (causal) or all S keys
+        for (int i = 0; i < qt.valid; ++i)
+          pairs += causal ? qs.pos0 + qs.stride * (qt.off + i) + 1 : S;
+      }
+    }
+    if (visible_pairs) visible_pairs[r] = pairs;
+    if (computed_tiles) computed_tiles[r] = tiles;
+  }
+  return RA_OK;
+}
+
+ra_status ring_attn_check_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int word = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&word, ra::g_dev_status, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, "reading device status");
+  if (word != 0) {
+    e = cudaMemcpyToSymbol(ra::g_dev_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing device status");
+    return fail(RA_ERR_DEVICE_TIMEOUT, "a kernel gave up on a bounded wait (status 0x%x)", word);
+  }
+  return RA_OK;
+}
+
+const char* ring_attn_last_error(void) { return g_last_error; }
+
+const char* ring_attn_version(void) { return "ring_attn 0.1.0 (sm_103a)"; }
+
+}  // extern "C"
