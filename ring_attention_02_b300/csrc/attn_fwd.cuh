@@ -39,6 +39,15 @@ namespace ra {
 
 enum { FWD_MODE_RING = 0, FWD_MODE_STEP = 1 };
 
+// Register budget: 384 threads launched at kRegsLaunch registers each; the
+// control warpgroup drops to kRegsControl and the two softmax warpgroups rise
+// to kRegsSoftmax, using exactly the launched total.
+constexpr int kRegsLaunch = 168;
+constexpr uint32_t kRegsControl = 88;
+constexpr uint32_t kRegsSoftmax = 208;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * kRegsLaunch,
+              "register split exceeds the launch budget");
+
 struct FwdParams {
   Geo g;
   int mode;            // FWD_MODE_RING: natural-order tensors, all blocks in ring order
@@ -80,86 +89,89 @@ struct __align__(1024) FwdSmem {
 };
 
 // Per-unit schedule facts every role derives identically.
-struct UnitInfo {
-  int b, h, hkv;
-  QTile qt[2];
-  int64_t qmax;        // largest query position of the unit
-  int ntiles[2];       // active key tiles per query tile
+struct UnitHead {
+  int b, h, hkv, shard, seg, pair;
 };
 
-__device__ __forceinline__ UnitInfo unit_info(const FwdParams& p, int64_t item) {
-  UnitInfo ui;
+__device__ __forceinline__ UnitHead unit_head(const FwdParams& p, int64_t item) {
+  UnitHead u;
   const Geo& g = p.g;
-  const int64_t bh = item % ((int64_t)g.B * g.H);
-  const int64_t u = item / ((int64_t)g.B * g.H);
-  ui.b = (int)(bh / g.H);
-  ui.h = (int)(bh % g.H);
-  ui.hkv = ui.h / (g.H / g.Hkv);
-  const bool step = p.mode == FWD_MODE_STEP;
-  Unit w = unit_of(g, u, step, p.step_r);
-  ui.qt[0] = make_qtile(g, w.shard, w.seg, 2 * w.pair);
-  ui.qt[1] = make_qtile(g, w.shard, w.seg, 2 * w.pair + 1);
-  ui.qmax = ui.qt[1].valid ? ui.qt[1].qmax : ui.qt[0].qmax;
-  if (ui.qt[0].valid && ui.qt[0].qmax > ui.qmax) ui.qmax = ui.qt[0].qmax;
-  for (int x = 0; x < 2; ++x) ui.ntiles[x] = (int)tile_work(g, ui.qt[x], step ? p.step_s : -1);
-  return ui;
+  const int bh_count = g.B * g.H;
+  const int bh = (int)(item % bh_count);
+  const int64_t unit = item / bh_count;
+  u.b = bh / g.H;
+  u.h = bh % g.H;
+  u.hkv = u.h / (g.H / g.Hkv);
+  Unit w = unit_of(g, unit, p.mode == FWD_MODE_STEP, p.step_r);
+  u.shard = w.shard;
+  u.seg = w.seg;
+  u.pair = w.pair;
+  return u;
 }
 
-// Iterator over the union of key tiles of a unit, in ring order.
+__device__ __forceinline__ int step_block(const FwdParams& p) {
+  return p.mode == FWD_MODE_STEP ? p.step_s : -1;
+}
+
+// Iterator over the union of the key tiles a unit multiplies, in ring order.
 struct KIter {
-  int t, t_end, sk, bt, nk;
-  int s;
+  int t, t_end, sk, bt, nk, s;
+  int qmax, shard;
   Seg seg;
 };
 
-__device__ __forceinline__ void kiter_setup(const FwdParams& p, const UnitInfo& ui, KIter& it) {
+__device__ __forceinline__ void kiter_setup(const FwdParams& p, int shard, int qmax, KIter& it) {
   it.t = 0;
   it.t_end = p.mode == FWD_MODE_STEP ? 1 : p.g.P;
   it.sk = 0;
   it.bt = 0;
-  it.s = p.mode == FWD_MODE_STEP ? p.step_s : ring_block(p.g, ui.qt[0].shard, 0);
+  it.qmax = qmax;
+  it.shard = shard;
+  it.s = p.mode == FWD_MODE_STEP ? p.step_s : ring_block(p.g, shard, 0);
   it.seg = segment_of(p.g, it.s, 0);
-  it.nk = visible_tiles(p.g, it.seg, ui.qmax);
+  it.nk = visible_tiles(p.g, it.seg, qmax);
 }
 
 // Advances to the next key tile; false when the schedule is exhausted.
-__device__ __forceinline__ bool kiter_next(const FwdParams& p, const UnitInfo& ui, KIter& it) {
+__device__ __forceinline__ bool kiter_next(const FwdParams& p, KIter& it) {
   while (it.bt >= it.nk) {
     it.bt = 0;
     if (++it.sk >= p.g.nseg) {
       it.sk = 0;
       if (++it.t >= it.t_end) return false;
-      it.s = ring_block(p.g, ui.qt[0].shard, it.t);
+      it.s = ring_block(p.g, it.shard, it.t);
     }
     it.seg = segment_of(p.g, it.s, it.sk);
-    it.nk = visible_tiles(p.g, it.seg, ui.qmax);
+    it.nk = visible_tiles(p.g, it.seg, it.qmax);
   }
   return true;
 }
 
-// Is key tile (it.seg, it.bt) visible to query tile x?
-__device__ __forceinline__ bool tile_active(const FwdParams& p, const UnitInfo& ui,
-                                            const KIter& it, int x) {
-  if (!ui.qt[x].valid) return false;
-  if (!p.g.causal) return true;
-  return it.seg.pos0 + it.seg.stride * ((int64_t)it.bt * kTile) <= ui.qt[x].qmax;
+// Position of the first key of the iterator's current tile.
+__device__ __forceinline__ int kiter_first_pos(const KIter& it) {
+  return it.seg.pos0 + it.seg.stride * (it.bt * kTile);
+}
+
+// Is the current key tile visible to a query tile whose last position is qmax?
+__device__ __forceinline__ bool visible_to(const FwdParams& p, const KIter& it, int valid,
+                                           int qmax) {
+  return valid && (!p.g.causal || kiter_first_pos(it) <= qmax);
 }
 
 // TMA coordinates (phase, row) of a tile starting at offset `off` of segment
-// (pos0, stride, local0) of shard `shard`, batch b.
-__device__ __forceinline__ void tile_coords(const FwdParams& p, int shard, int64_t pos0,
-                                            int64_t local0, int64_t off, int b, int& phase,
-                                            int& row) {
+// (pos0, local0) of shard `shard`, batch b.
+__device__ __forceinline__ void tile_coords(const FwdParams& p, int shard, int pos0, int local0,
+                                            int off, int b, int& phase, int& row) {
   const Geo& g = p.g;
   if (p.mode == FWD_MODE_STEP) {
     phase = 0;
-    row = (int)((int64_t)b * g.n + local0 + off);
+    row = b * g.n + local0 + off;
   } else if (g.layout == LAYOUT_STRIPED) {
     phase = shard;
-    row = (int)((int64_t)b * g.n + off);
+    row = b * g.n + off;
   } else {
     phase = 0;
-    row = (int)((int64_t)b * g.S + pos0 + off);
+    row = b * g.S + pos0 + off;
   }
 }
 
@@ -203,6 +215,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  const Geo& g = p.g;
+  const int sblk = step_block(p);
 
   // Static "snake" assignment of the longest-first item list: round k gives
   // CTA c item k*G + c (k even) or k*G + G-1-c (k odd).
@@ -210,132 +224,148 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int64_t c = blockIdx.x;
   auto item_at = [&](int64_t k) -> int64_t { return k * G + ((k & 1) ? (G - 1 - c) : c); };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  if (warp < 4) {
+    // Producer / MMA / idle warps give registers to the two softmax warpgroups.
+    regs_dec<kRegsControl>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      uint32_t q_ph[2] = {0, 0};
+      uint32_t q_ph0 = 0, q_ph1 = 0;
       uint32_t kst = 0, k_ph = 0, vst = 0, v_ph = 0;
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
-        UnitInfo ui = unit_info(p, item);
+        const UnitHead u = unit_head(p, item);
+        const QTile qa = make_qtile(g, u.shard, u.seg, 2 * u.pair);
+        const QTile qb = make_qtile(g, u.shard, u.seg, 2 * u.pair + 1);
+        const int na = tile_work(g, qa, sblk), nb = tile_work(g, qb, sblk);
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (ui.ntiles[x] == 0) continue;
-          if (!mbar_wait(smem_u32(&sm.q_empty[x]), q_ph[x] ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
+          const QTile& qt = x ? qb : qa;
+          if ((x ? nb : na) == 0) continue;
+          uint32_t& ph = x ? q_ph1 : q_ph0;
+          if (!mbar_wait(smem_u32(&sm.q_empty[x]), ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
             goto done;
-          q_ph[x] ^= 1;
+          ph ^= 1;
           const uint32_t bar = smem_u32(&sm.q_full[x]);
           mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
           int phase, row;
-          const QTile& qt = ui.qt[x];
-          tile_coords(p, qt.shard, qt.pos0, qt.local0, qt.off, ui.b, phase, row);
+          tile_coords(p, qt.shard, qt.pos0, qt.local0, qt.off, u.b, phase, row);
+#pragma unroll
           for (int st = 0; st < Cfg::kSubTiles; ++st)
-            tma_load_4d(smem_u32(sm.q[x]) + st * (kTile * 128), &tm_q, bar, 64 * st, ui.h, phase,
+            tma_load_4d(smem_u32(sm.q[x]) + st * (kTile * 128), &tm_q, bar, 64 * st, u.h, phase,
                         row, pol_q);
         }
         KIter it;
-        kiter_setup(p, ui, it);
-        while (kiter_next(p, ui, it)) {
+        kiter_setup(p, u.shard, qb.valid && qb.qmax > qa.qmax ? qb.qmax : qa.qmax, it);
+        while (kiter_next(p, it)) {
           int phase, row;
-          tile_coords(p, it.s, it.seg.pos0, it.seg.local0, (int64_t)it.bt * kTile, ui.b, phase,
-                      row);
+          tile_coords(p, it.s, it.seg.pos0, it.seg.local0, it.bt * kTile, u.b, phase, row);
           if (!mbar_wait(smem_u32(&sm.k_empty[kst]), k_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
             goto done;
           uint32_t bar = smem_u32(&sm.k_full[kst]);
           mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
+#pragma unroll
           for (int st = 0; st < Cfg::kSubTiles; ++st)
-            tma_load_4d(smem_u32(sm.k[kst]) + st * (kTile * 128), &tm_k, bar, 64 * st, ui.hkv,
+            tma_load_4d(smem_u32(sm.k[kst]) + st * (kTile * 128), &tm_k, bar, 64 * st, u.hkv,
                         phase, row, pol_kv);
           if (++kst == Cfg::kKStages) { kst = 0; k_ph ^= 1; }
           if (!mbar_wait(smem_u32(&sm.v_empty[vst]), v_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
             goto done;
           bar = smem_u32(&sm.v_full[vst]);
           mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
+#pragma unroll
           for (int st = 0; st < Cfg::kSubTiles; ++st)
-            tma_load_4d(smem_u32(sm.v[vst]) + st * (kTile * 128), &tm_v, bar, 64 * st, ui.hkv,
+            tma_load_4d(smem_u32(sm.v[vst]) + st * (kTile * 128), &tm_v, bar, 64 * st, u.hkv,
                         phase, row, pol_kv);
           if (++vst == Cfg::kVStages) { vst = 0; v_ph ^= 1; }
           ++it.bt;
         }
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16(128, D, false, true);
-      uint32_t q_ph[2] = {0, 0}, p_ph[2] = {0, 0};
+      uint32_t q_ph0 = 0, q_ph1 = 0, p_ph0 = 0, p_ph1 = 0;
       uint32_t kst = 0, k_ph = 0, vst = 0, v_ph = 0;
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
-        UnitInfo ui = unit_info(p, item);
-        if (ui.ntiles[0] + ui.ntiles[1] == 0) continue;
+        const UnitHead u = unit_head(p, item);
+        const QTile qa = make_qtile(g, u.shard, u.seg, 2 * u.pair);
+        const QTile qb = make_qtile(g, u.shard, u.seg, 2 * u.pair + 1);
+        const int na = tile_work(g, qa, sblk), nb = tile_work(g, qb, sblk);
+        if (na + nb == 0) continue;
         if (p.shard_tiles != nullptr)
-          atomicAdd(p.shard_tiles + ui.qt[0].shard,
-                    static_cast<unsigned long long>(ui.ntiles[0] + ui.ntiles[1]));
-        int cnt_s[2] = {0, 0}, cnt_pv[2] = {0, 0};
-        bool pend[2] = {false, false};   // a P V of the previous key tile is owed
+          atomicAdd(p.shard_tiles + u.shard, static_cast<unsigned long long>(na + nb));
+        int cnt_s0 = 0, cnt_s1 = 0, cnt_pv0 = 0, cnt_pv1 = 0;
+        bool pend0 = false, pend1 = false;   // a P V of the previous key tile is owed
         int prev_vst = -1;
         KIter it;
-        kiter_setup(p, ui, it);
-        bool more = kiter_next(p, ui, it);
+        kiter_setup(p, u.shard, qb.valid && qb.qmax > qa.qmax ? qb.qmax : qa.qmax, it);
+        bool more = kiter_next(p, it);
         while (true) {
-          bool act[2] = {false, false};
+          bool act0 = false, act1 = false;
           if (more) {
-            act[0] = tile_active(p, ui, it, 0);
-            act[1] = tile_active(p, ui, it, 1);
+            act0 = visible_to(p, it, qa.valid, qa.qmax);
+            act1 = visible_to(p, it, qb.valid, qb.qmax);
             if (!mbar_wait(smem_u32(&sm.k_full[kst]), k_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
               goto done;
             tc_fence_after();
           }
-          if (pend[0] || pend[1]) {
+          if (pend0 || pend1) {
             if (!mbar_wait(smem_u32(&sm.v_full[prev_vst]), v_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
               goto done;
             tc_fence_after();
           }
+#pragma unroll
           for (int x = 0; x < 2; ++x) {
-            if (pend[x]) {
+            bool& pend = x ? pend1 : pend0;
+            int& cnt_pv = x ? cnt_pv1 : cnt_pv0;
+            int& cnt_s = x ? cnt_s1 : cnt_s0;
+            uint32_t& p_ph = x ? p_ph1 : p_ph0;
+            uint32_t& q_ph = x ? q_ph1 : q_ph0;
+            const int nx = x ? nb : na;
+            if (pend) {
               // O_x += P_x V_prev
-              if (!mbar_wait(smem_u32(&sm.p_full[x]), p_ph[x], RA_DEV_TIMEOUT_MMA, abort_flag))
+              if (!mbar_wait(smem_u32(&sm.p_full[x]), p_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
                 goto done;
-              p_ph[x] ^= 1;
+              p_ph ^= 1;
               tc_fence_after();
               const uint32_t vb = smem_u32(sm.v[prev_vst]);
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk)
                 mma_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8,
                        sdesc_sw128(vb + kk * 2048, kTile * 128, 1024), id_pv,
-                       (cnt_pv[x] > 0 || kk > 0) ? 1u : 0u);
-              ++cnt_pv[x];
-              pend[x] = false;
-              if (cnt_pv[x] == ui.ntiles[x]) mma_commit(smem_u32(&sm.o_full[x]));
+                       (cnt_pv > 0 || kk > 0) ? 1u : 0u);
+              ++cnt_pv;
+              pend = false;
+              if (cnt_pv == nx) mma_commit(smem_u32(&sm.o_full[x]));
             }
-            if (more && act[x]) {
-              if (cnt_s[x] == 0) {
-                if (!mbar_wait(smem_u32(&sm.q_full[x]), q_ph[x], RA_DEV_TIMEOUT_MMA, abort_flag))
+            if (more && (x ? act1 : act0)) {
+              if (cnt_s == 0) {
+                if (!mbar_wait(smem_u32(&sm.q_full[x]), q_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
                   goto done;
-                q_ph[x] ^= 1;
+                q_ph ^= 1;
                 tc_fence_after();
               }
               // S_x = Q_x K^T
-              const uint32_t qb = smem_u32(sm.q[x]);
-              const uint32_t kb = smem_u32(sm.k[kst]);
+              const uint32_t qbase = smem_u32(sm.q[x]);
+              const uint32_t kbase = smem_u32(sm.k[kst]);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-                mma_ss(tmem + col_s(x), sdesc_sw128(qb + off, 16, 1024),
-                       sdesc_sw128(kb + off, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
+                mma_ss(tmem + col_s(x), sdesc_sw128(qbase + off, 16, 1024),
+                       sdesc_sw128(kbase + off, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
               }
               mma_commit(smem_u32(&sm.s_full[x]));
-              ++cnt_s[x];
-              if (cnt_s[x] == ui.ntiles[x]) mma_commit(smem_u32(&sm.q_empty[x]));
-              pend[x] = true;
+              ++cnt_s;
+              if (cnt_s == nx) mma_commit(smem_u32(&sm.q_empty[x]));
+              pend = true;
             }
           }
           if (prev_vst >= 0) {
@@ -348,11 +378,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (++kst == Cfg::kKStages) { kst = 0; k_ph ^= 1; }
           prev_vst = (int)vst;
           ++it.bt;
-          more = kiter_next(p, ui, it);
+          more = kiter_next(p, it);
         }
       }
     }
-  } else if (warp >= 4) {
+  } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int x = (warp - 4) / 4;                 // query tile A (0) or B (1)
     const int quarter = warp % 4;                 // TMEM lanes [32*quarter, +32)
@@ -361,35 +392,42 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t t_s = tmem + lane_addr + col_s(x);
     const uint32_t t_o = tmem + lane_addr + col_o(x);
     const float sl2 = p.scale_log2;
+    const bool pos_scale = sl2 >= 0.f;
     uint32_t s_ph = 0, o_ph = 0;
     for (int64_t k = 0;; ++k) {
       const int64_t item = item_at(k);
       if (item >= p.num_items) break;
-      UnitInfo ui = unit_info(p, item);
-      const QTile& qt = ui.qt[x];
+      const UnitHead u = unit_head(p, item);
+      const QTile qt = make_qtile(g, u.shard, u.seg, 2 * u.pair + x);
       if (!qt.valid) continue;
+      int qmax_u = qt.qmax;
+      {
+        const QTile other = make_qtile(g, u.shard, u.seg, 2 * u.pair + (x ^ 1));
+        if (other.valid && other.qmax > qmax_u) qmax_u = other.qmax;
+      }
+      const int ntiles = tile_work(g, qt, sblk);
       const bool row_ok = row < qt.valid;
-      const int64_t qpos = qt.pos0 + qt.stride * (qt.off + row);
+      const int qpos = qt.pos0 + qt.stride * (qt.off + row);
       float m_run = -INFINITY;   // running max, scaled log2 units
       float l_run = 0.f;         // running normaliser
-      if (ui.ntiles[x] > 0) {
+      if (ntiles > 0) {
         KIter it;
-        kiter_setup(p, ui, it);
-        while (kiter_next(p, ui, it)) {
-          if (!tile_active(p, ui, it, x)) { ++it.bt; continue; }
-          const int64_t k0 = (int64_t)it.bt * kTile;
-          const int64_t kleft = it.seg.len - k0;
-          const int kvalid = kleft < kTile ? (int)kleft : kTile;
+        kiter_setup(p, u.shard, qmax_u, it);
+        while (kiter_next(p, it)) {
+          if (!visible_to(p, it, 1, qt.qmax)) { ++it.bt; continue; }
+          const int k0 = it.bt * kTile;
+          const int kleft = it.seg.len - k0;
+          const int kvalid = kleft < kTile ? kleft : kTile;
           int lim = kvalid;
           bool masked = kvalid < kTile;
-          if (p.g.causal) {
-            const int64_t kmax = it.seg.pos0 + it.seg.stride * (k0 + kvalid - 1);
+          if (g.causal) {
+            const int kmax = it.seg.pos0 + it.seg.stride * (k0 + kvalid - 1);
             if (kmax > qt.qmin) masked = true;
-            int64_t cl = count_le(it.seg, qpos) - k0;
-            lim = cl < 0 ? 0 : (cl > kvalid ? kvalid : (int)cl);
+            const int cl = count_le(it.seg, qpos) - k0;
+            lim = cl < 0 ? 0 : (cl > kvalid ? kvalid : cl);
           }
-          if (!__all_sync(0xffffffffu,
-                          mbar_wait(smem_u32(&sm.s_full[x]), s_ph, RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[x]), s_ph,
+                                                 RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
             goto done;
           s_ph ^= 1;
           tc_fence_after();
@@ -402,21 +440,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int i = 0; i < 32; ++i) s[cch * 32 + i] = __uint_as_float(r[i]);
           }
           tmem_wait_ld();
-          // row extreme of the raw scores over the visible columns
+          // Hidden columns take the value that never wins the row extreme
+          // (-inf for a positive scale, +inf for a negative one).
+          if (masked) {
+            const float neutral = pos_scale ? -INFINITY : INFINITY;
+#pragma unroll
+            for (int i = 0; i < kTile; ++i) s[i] = i < lim ? s[i] : neutral;
+          }
           float mt;
-          if (sl2 >= 0.f) {
+          if (pos_scale) {
             mt = -INFINITY;
-            if (masked) {
 #pragma unroll
-              for (int i = 0; i < kTile; ++i) mt = fmaxf(mt, i < lim ? s[i] : -INFINITY);
-            } else {
-#pragma unroll
-              for (int i = 0; i < kTile; ++i) mt = fmaxf(mt, s[i]);
-            }
+            for (int i = 0; i < kTile; i += 2) mt = max3f(mt, s[i], s[i + 1]);
           } else {
             mt = INFINITY;
 #pragma unroll
-            for (int i = 0; i < kTile; ++i) mt = fminf(mt, i < lim ? s[i] : INFINITY);
+            for (int i = 0; i < kTile; i += 2) mt = min3f(mt, s[i], s[i + 1]);
           }
           const bool any = masked ? lim > 0 : true;
           const float m_tile = any ? mt * sl2 : -INFINITY;
@@ -432,95 +471,100 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           if (__any_sync(0xffffffffu, need)) {
             l_run *= corr;
+            const float2 c2 = make_float2(corr, corr);
 #pragma unroll
             for (int cch = 0; cch < D / 32; ++cch) {
               uint32_t r[32];
               tmem_ld32(t_o + cch * 32, r);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+              for (int i = 0; i < 32; i += 2) {
+                float2 o2 = mul2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2);
+                r[i] = __float_as_uint(o2.x);
+                r[i + 1] = __float_as_uint(o2.y);
+              }
               tmem_st32(t_o + cch * 32, r);
             }
           }
-          const float m_use = m_run == -INFINITY ? 0.f : m_run;
-          float lsum = 0.f;
+          const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+          const float2 sl2_2 = make_float2(sl2, sl2);
+          const float2 negm2 = make_float2(neg_m, neg_m);
+          float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int cch = 0; cch < 4; ++cch) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int c0 = cch * 32 + 2 * i;
-              float p0 = ex2_approx(fmaf(s[c0], sl2, -m_use));
-              float p1 = ex2_approx(fmaf(s[c0 + 1], sl2, -m_use));
+              const float2 t2 = fma2(make_float2(s[c0], s[c0 + 1]), sl2_2, negm2);
+              float p0 = ex2_approx(t2.x);
+              float p1 = ex2_approx(t2.y);
               if (masked) {
                 p0 = c0 < lim ? p0 : 0.f;
                 p1 = c0 + 1 < lim ? p1 : 0.f;
               }
-              lsum += p0 + p1;
+              sum2 = add2(sum2, make_float2(p0, p1));
               pk[i] = pack_bf16x2(p0, p1);
             }
             tmem_st16(t_s + cch * 16, pk);
           }
-          l_run += lsum;
+          l_run += sum2.x + sum2.y;
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(smem_u32(&sm.p_full[x]));
           ++it.bt;
         }
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(smem_u32(&sm.o_full[x]), o_ph, RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_full[x]), o_ph,
+                                               RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
           goto done;
         o_ph ^= 1;
         tc_fence_after();
       }
       // ---- epilogue: out = O / l, lse = (m + log2 l) * ln 2
-      {
-        const bool has = ui.ntiles[x] > 0 && l_run > 0.f;
-        const float inv_l = has ? 1.f / l_run : 0.f;
-        int64_t orow, lidx;
-        const Geo& g = p.g;
-        if (p.mode == FWD_MODE_STEP) {
-          const int64_t j = qt.local0 + qt.off + row;
-          orow = ((int64_t)ui.b * g.n + j) * g.H + ui.h;
-          lidx = ((int64_t)ui.b * g.H + ui.h) * g.n + j;
-        } else {
-          orow = ((int64_t)ui.b * g.S + qpos) * g.H + ui.h;
-          lidx = ((int64_t)ui.b * g.H + ui.h) * g.S + qpos;
-        }
-#pragma unroll
-        for (int cch = 0; cch < D / 32; ++cch) {
-          uint32_t r[32];
-          if (ui.ntiles[x] > 0) {
-            tmem_ld32(t_o + cch * 32, r);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;
-          }
-          if (row_ok) {
-            if (p.out_f32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D + cch * 32);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l,
-                                     __uint_as_float(r[4 * i + 1]) * inv_l,
-                                     __uint_as_float(r[4 * i + 2]) * inv_l,
-                                     __uint_as_float(r[4 * i + 3]) * inv_l);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * D + cch * 32);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(
-                    pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
-                    pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
-                    pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
-                    pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
-            }
-          }
-        }
-        if (row_ok && p.lse != nullptr)
-          p.lse[lidx] = has ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+      const bool has = ntiles > 0 && l_run > 0.f;
+      const float inv_l = has ? 1.f / l_run : 0.f;
+      int64_t orow, lidx;
+      if (p.mode == FWD_MODE_STEP) {
+        const int j = qt.local0 + qt.off + row;
+        orow = ((int64_t)u.b * g.n + j) * g.H + u.h;
+        lidx = ((int64_t)u.b * g.H + u.h) * g.n + j;
+      } else {
+        orow = ((int64_t)u.b * g.S + qpos) * g.H + u.h;
+        lidx = ((int64_t)u.b * g.H + u.h) * g.S + qpos;
       }
+#pragma unroll
+      for (int cch = 0; cch < D / 32; ++cch) {
+        uint32_t r[32];
+        if (ntiles > 0) {
+          tmem_ld32(t_o + cch * 32, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (row_ok) {
+          if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D + cch * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l,
+                                   __uint_as_float(r[4 * i + 1]) * inv_l,
+                                   __uint_as_float(r[4 * i + 2]) * inv_l,
+                                   __uint_as_float(r[4 * i + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow * D + cch * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(
+                  pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l),
+                  pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l),
+                  pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l),
+                  pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l));
+          }
+        }
+      }
+      if (row_ok && p.lse != nullptr)
+        p.lse[lidx] = has ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     }
   }
 

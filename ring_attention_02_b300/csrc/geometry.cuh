@@ -22,27 +22,28 @@ namespace ra {
 constexpr int kTile = 128;
 enum { LAYOUT_CONTIGUOUS = 0, LAYOUT_STRIPED = 1, LAYOUT_ZIGZAG = 2 };
 
+// Positions, lengths and offsets are int32: the host rejects B*S >= 2^31.
 struct Geo {
   int B, H, Hkv, P, layout, causal;
-  int64_t S, n, C;
+  int S, n, C;
   int nseg;          // segments per shard (1, or 2 for zig-zag)
-  int64_t seglen;    // slots per segment
+  int seglen;        // slots per segment
   int ntile;         // tiles per segment = ceil(seglen / 128)
   int npair;         // tile pairs per segment = ceil(ntile / 2)
 };
 
 struct Seg {
-  int64_t pos0, stride, len, local0;
+  int pos0, stride, len, local0;
 };
 
 __host__ __device__ inline Geo make_geo(int B, int H, int Hkv, int64_t S, int P, int layout,
                                         int causal) {
   Geo g;
   g.B = B; g.H = H; g.Hkv = Hkv; g.P = P; g.layout = layout; g.causal = causal;
-  g.S = S; g.n = S / P; g.C = S / (2 * (int64_t)P);
+  g.S = (int)S; g.n = (int)(S / P); g.C = (int)(S / (2 * (int64_t)P));
   g.nseg = layout == LAYOUT_ZIGZAG ? 2 : 1;
   g.seglen = layout == LAYOUT_ZIGZAG ? g.C : g.n;
-  g.ntile = (int)((g.seglen + kTile - 1) / kTile);
+  g.ntile = (g.seglen + kTile - 1) / kTile;
   g.npair = (g.ntile + 1) / 2;
   return g;
 }
@@ -50,21 +51,21 @@ __host__ __device__ inline Geo make_geo(int B, int H, int Hkv, int64_t S, int P,
 __host__ __device__ inline Seg segment_of(const Geo& g, int shard, int seg) {
   Seg s;
   if (g.layout == LAYOUT_ZIGZAG) {
-    int64_t chunk = seg == 0 ? shard : 2 * (int64_t)g.P - 1 - shard;
+    int chunk = seg == 0 ? shard : 2 * g.P - 1 - shard;
     s.pos0 = chunk * g.C; s.stride = 1; s.len = g.C; s.local0 = seg * g.C;
   } else if (g.layout == LAYOUT_STRIPED) {
     s.pos0 = shard; s.stride = g.P; s.len = g.n; s.local0 = 0;
   } else {
-    s.pos0 = (int64_t)shard * g.n; s.stride = 1; s.len = g.n; s.local0 = 0;
+    s.pos0 = shard * g.n; s.stride = 1; s.len = g.n; s.local0 = 0;
   }
   return s;
 }
 
 // Number of slots of segment k whose position is <= x (positions increase
 // along the segment, so these are its first count_le slots).
-__host__ __device__ inline int64_t count_le(const Seg& k, int64_t x) {
+__host__ __device__ inline int count_le(const Seg& k, int x) {
   if (x < k.pos0) return 0;
-  int64_t c = (x - k.pos0) / k.stride + 1;
+  int c = (x - k.pos0) / k.stride + 1;
   return c < k.len ? c : k.len;
 }
 
@@ -72,30 +73,30 @@ __host__ __device__ inline int64_t count_le(const Seg& k, int64_t x) {
 __host__ __device__ inline int64_t position_of(const Geo& g, int shard, int64_t j) {
   int seg = (g.layout == LAYOUT_ZIGZAG && j >= g.C) ? 1 : 0;
   Seg s = segment_of(g, shard, seg);
-  return s.pos0 + s.stride * (j - s.local0);
+  return (int64_t)s.pos0 + (int64_t)s.stride * (j - s.local0);
 }
 
 // One 128-slot query tile.
 struct QTile {
   int valid;        // 0 if the tile does not exist, else number of rows (1..128)
-  int shard, seg;
-  int64_t off;      // first slot offset within the segment
-  int64_t pos0, stride, local0;
-  int64_t qmin, qmax;
+  int shard;
+  int off;          // first slot offset within the segment
+  int pos0, stride, local0;
+  int qmin, qmax;
 };
 
 __host__ __device__ inline QTile make_qtile(const Geo& g, int shard, int seg, int tile) {
   QTile q;
-  q.shard = shard; q.seg = seg;
+  q.shard = shard;
   Seg s = segment_of(g, shard, seg);
-  q.off = (int64_t)tile * kTile;
+  q.off = tile * kTile;
   q.pos0 = s.pos0; q.stride = s.stride; q.local0 = s.local0;
   if (tile >= g.ntile || q.off >= s.len) {
     q.valid = 0; q.qmin = 0; q.qmax = -1;
     return q;
   }
-  int64_t rows = s.len - q.off;
-  q.valid = rows < kTile ? (int)rows : kTile;
+  int rows = s.len - q.off;
+  q.valid = rows < kTile ? rows : kTile;
   q.qmin = s.pos0 + s.stride * q.off;
   q.qmax = s.pos0 + s.stride * (q.off + q.valid - 1);
   return q;
@@ -150,16 +151,16 @@ __host__ __device__ inline int ring_block(const Geo& g, int r, int t) {
   return s < 0 ? s + g.P : s;
 }
 
-__host__ __device__ inline int visible_tiles(const Geo& g, const Seg& k, int64_t qmax) {
-  int64_t c = g.causal ? count_le(k, qmax) : k.len;
-  return (int)((c + kTile - 1) / kTile);
+__host__ __device__ inline int visible_tiles(const Geo& g, const Seg& k, int qmax) {
+  int c = g.causal ? count_le(k, qmax) : k.len;
+  return (c + kTile - 1) / kTile;
 }
 
 // Number of key tiles a query tile multiplies over the whole schedule
 // (ring mode) or against block s only (step mode, s >= 0).
-__host__ __device__ inline int64_t tile_work(const Geo& g, const QTile& q, int step_s) {
+__host__ __device__ inline int tile_work(const Geo& g, const QTile& q, int step_s) {
   if (!q.valid) return 0;
-  int64_t total = 0;
+  int total = 0;
   const int t_end = step_s >= 0 ? 1 : g.P;
   for (int t = 0; t < t_end; ++t) {
     int s = step_s >= 0 ? step_s : ring_block(g, q.shard, t);

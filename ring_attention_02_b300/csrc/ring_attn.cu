@@ -134,8 +134,16 @@ ra_status launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   const size_t smem = sizeof(ra::FwdSmem<D>) + 1024;
   const int di = D == 128 ? 1 : 0;
   if (!dev->fwd_attr_set[di]) {
-    cudaError_t e = cudaFuncSetAttribute(ra::attn_fwd_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // The kernel moves registers between warpgroups (setmaxnreg); that only
+    // completes if the launch holds exactly the budget the split assumes.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, ra::attn_fwd_kernel<D>);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(fwd)");
+    if (fa.numRegs != ra::kRegsLaunch)
+      return fail(RA_ERR_UNSUPPORTED, "forward kernel built with %d registers/thread, expected %d",
+                  fa.numRegs, ra::kRegsLaunch);
+    e = cudaFuncSetAttribute(ra::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd smem)");
     dev->fwd_attr_set[di] = true;
   }

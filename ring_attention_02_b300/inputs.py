@@ -59,8 +59,18 @@ MILLION = Workload("causal-B1H8Hkv1S1048576D128P32", 1, 8, 1, 1048576, 128, 32, 
 TRAIN_32K = Workload("train-B2H16S32768D128P8", 2, 16, 16, 32768, 128, 8, "zigzag", True,
                      backward=True)
 WORKLOADS = [TINY, CAUSAL_8K, GQA_128K, MILLION, TRAIN_32K]
+# A mid-size causal forward for profiler captures: 192 MiB of q/k/v (larger
+# than the 126 MB L2) and a few milliseconds per launch.
+PROFILE_32K = Workload("causal-B1H8S32768D128P8", 1, 8, 8, 32768, 128, 8, "zigzag", True)
 # The headline forward: the 128k GQA shapes with the zig-zag layout.
 HEADLINE = GQA_128K.with_layout("zigzag")
+
+
+def by_name(name: str) -> Workload:
+    for w in WORKLOADS + [HEADLINE, PROFILE_32K]:
+        if w.name == name:
+            return w
+    raise KeyError(name)
 
 
 def _randn_bf16(shape, seed: int, device) -> torch.Tensor:
