@@ -418,11 +418,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const int k0 = it.bt * kTile;
           const int kleft = it.seg.len - k0;
           const int kvalid = kleft < kTile ? kleft : kTile;
-          int lim = kvalid;
           bool masked = kvalid < kTile;
-          if (g.causal) {
-            const int kmax = it.seg.pos0 + it.seg.stride * (k0 + kvalid - 1);
-            if (kmax > qt.qmin) masked = true;
+          if (g.causal && it.seg.pos0 + it.seg.stride * (k0 + kvalid - 1) > qt.qmin) masked = true;
+          int lim = kvalid;
+          if (masked && g.causal) {
             const int cl = count_le(it.seg, qpos) - k0;
             lim = cl < 0 ? 0 : (cl > kvalid ? kvalid : cl);
           }
@@ -440,73 +439,114 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int i = 0; i < 32; ++i) s[cch * 32 + i] = __uint_as_float(r[i]);
           }
           tmem_wait_ld();
-          // Hidden columns take the value that never wins the row extreme
-          // (-inf for a positive scale, +inf for a negative one).
-          if (masked) {
-            const float neutral = pos_scale ? -INFINITY : INFINITY;
-#pragma unroll
-            for (int i = 0; i < kTile; ++i) s[i] = i < lim ? s[i] : neutral;
-          }
-          float mt;
-          if (pos_scale) {
-            mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < kTile; i += 2) mt = max3f(mt, s[i], s[i + 1]);
-          } else {
-            mt = INFINITY;
-#pragma unroll
-            for (int i = 0; i < kTile; i += 2) mt = min3f(mt, s[i], s[i + 1]);
-          }
-          const bool any = masked ? lim > 0 : true;
-          const float m_tile = any ? mt * sl2 : -INFINITY;
-          // lazy rescale: only when the max rises by more than 8 (log2 units)
-          float corr = 1.f;
-          bool need = false;
-          if (m_run == -INFINITY) {
-            m_run = m_tile;
-          } else if (m_tile > m_run + 8.f) {
-            corr = ex2_approx(m_run - m_tile);
-            m_run = m_tile;
-            need = true;
-          }
-          if (__any_sync(0xffffffffu, need)) {
-            l_run *= corr;
-            const float2 c2 = make_float2(corr, corr);
-#pragma unroll
-            for (int cch = 0; cch < D / 32; ++cch) {
-              uint32_t r[32];
-              tmem_ld32(t_o + cch * 32, r);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                float2 o2 = mul2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2);
-                r[i] = __float_as_uint(o2.x);
-                r[i + 1] = __float_as_uint(o2.y);
-              }
-              tmem_st32(t_o + cch * 32, r);
-            }
-          }
-          const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-          const float2 sl2_2 = make_float2(sl2, sl2);
-          const float2 negm2 = make_float2(neg_m, neg_m);
           float2 sum2 = make_float2(0.f, 0.f);
+          bool done_p = false;
+          if (!masked && pos_scale && m_run != -INFINITY) {
+            // Speculative pass: exponentials against the running max while the
+            // tile max is gathered alongside.  Valid unless this tile raises the
+            // max by more than 8 (then redone below), since P then stays < 2^8.
+            const float2 sl2_2 = make_float2(sl2, sl2);
+            const float2 negm2 = make_float2(-m_run, -m_run);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int cch = 0; cch < 4; ++cch) {
-            uint32_t pk[16];
+            for (int cch = 0; cch < 4; ++cch) {
+              uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int c0 = cch * 32 + 2 * i;
-              const float2 t2 = fma2(make_float2(s[c0], s[c0 + 1]), sl2_2, negm2);
-              float p0 = ex2_approx(t2.x);
-              float p1 = ex2_approx(t2.y);
-              if (masked) {
-                p0 = c0 < lim ? p0 : 0.f;
-                p1 = c0 + 1 < lim ? p1 : 0.f;
+              for (int i = 0; i < 16; ++i) {
+                const int c0 = cch * 32 + 2 * i;
+                mx[i % 4] = max3f(mx[i % 4], s[c0], s[c0 + 1]);
+                const float2 t2 = fma2(make_float2(s[c0], s[c0 + 1]), sl2_2, negm2);
+                const float p0 = ex2_approx(t2.x);
+                const float p1 = ex2_approx(t2.y);
+                acc[i % 4] = add2(acc[i % 4], make_float2(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
               }
-              sum2 = add2(sum2, make_float2(p0, p1));
-              pk[i] = pack_bf16x2(p0, p1);
+              tmem_st16(t_s + cch * 16, pk);
             }
-            tmem_st16(t_s + cch * 16, pk);
+            const float m_tile = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
+            const bool ok = !(m_tile > m_run + 8.f);
+            if (__all_sync(0xffffffffu, ok)) {
+              sum2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+              done_p = true;
+            }
+          }
+          if (!done_p) {
+            // Exact pass: row extreme first.  Hidden columns take the value that
+            // never wins it (-inf for a positive scale, +inf for a negative one).
+            if (masked) {
+              const float neutral = pos_scale ? -INFINITY : INFINITY;
+#pragma unroll
+              for (int i = 0; i < kTile; ++i) s[i] = i < lim ? s[i] : neutral;
+            }
+            float mq[4];
+            if (pos_scale) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) mq[j] = -INFINITY;
+#pragma unroll
+              for (int i = 0; i < kTile; i += 2) mq[(i / 2) % 4] = max3f(mq[(i / 2) % 4], s[i], s[i + 1]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) mq[j] = INFINITY;
+#pragma unroll
+              for (int i = 0; i < kTile; i += 2) mq[(i / 2) % 4] = min3f(mq[(i / 2) % 4], s[i], s[i + 1]);
+            }
+            const float mt = pos_scale ? max3f(mq[0], mq[1], fmaxf(mq[2], mq[3]))
+                                       : min3f(mq[0], mq[1], fminf(mq[2], mq[3]));
+            const bool any = masked ? lim > 0 : true;
+            const float m_tile = any ? mt * sl2 : -INFINITY;
+            // lazy rescale: only when the max rises by more than 8 (log2 units)
+            float corr = 1.f;
+            bool need = false;
+            if (m_run == -INFINITY) {
+              m_run = m_tile;
+            } else if (m_tile > m_run + 8.f) {
+              corr = ex2_approx(m_run - m_tile);
+              m_run = m_tile;
+              need = true;
+            }
+            if (__any_sync(0xffffffffu, need)) {
+              l_run *= corr;
+              const float2 c2 = make_float2(corr, corr);
+#pragma unroll
+              for (int cch = 0; cch < D / 32; ++cch) {
+                uint32_t r[32];
+                tmem_ld32(t_o + cch * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                  float2 o2 = mul2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2);
+                  r[i] = __float_as_uint(o2.x);
+                  r[i + 1] = __float_as_uint(o2.y);
+                }
+                tmem_st32(t_o + cch * 32, r);
+              }
+            }
+            const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+            const float2 sl2_2 = make_float2(sl2, sl2);
+            const float2 negm2 = make_float2(neg_m, neg_m);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+#pragma unroll
+            for (int cch = 0; cch < 4; ++cch) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int c0 = cch * 32 + 2 * i;
+                const float2 t2 = fma2(make_float2(s[c0], s[c0 + 1]), sl2_2, negm2);
+                float p0 = ex2_approx(t2.x);
+                float p1 = ex2_approx(t2.y);
+                if (masked) {
+                  p0 = c0 < lim ? p0 : 0.f;
+                  p1 = c0 + 1 < lim ? p1 : 0.f;
+                }
+                acc[i % 4] = add2(acc[i % 4], make_float2(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+              tmem_st16(t_s + cch * 16, pk);
+            }
+            sum2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
           }
           l_run += sum2.x + sum2.y;
           tmem_wait_st();
