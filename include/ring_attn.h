@@ -117,8 +117,16 @@ ra_status ring_attn_fwd_counted(const void* q, const void* k, const void* v, voi
  *   P = exp(scale q k^T - lse), delta = rowsum(dout * out),
  *   dv = P^T dout, dS = P * (dout v^T - delta), dq = scale dS k, dk = scale dS^T q,
  * with dk, dv summed over the H/Hkv query heads sharing a key/value head.
- *   out, lse: the forward's outputs (out bf16).  dq, dk, dv: bf16 outputs.
- * Uses an fp32 workspace of B*S*H*D*4 + B*H*S*4 bytes (cudaMallocAsync).
+ *   out, lse: the forward's outputs (out bf16, lse [B][H][S] fp32).
+ *   dout: [B][S][H][D] bf16.  dq [B][S][H][D], dk/dv [B][S][Hkv][D]: bf16 outputs,
+ *   every element written.
+ * Same size, layout and scale rules as ring_attn_fwd (out_dtype bf16 only).
+ * The key/value blocks meet the query shards in ring order; dq is computed in
+ * a separate pass over the query tiles, so no atomics are used and the
+ * result is deterministic.  Takes a transient fp32 workspace of
+ * 8 * B * H * P * T * 128 bytes (T = 128-slot tiles per shard, counted per
+ * zig-zag chunk) with cudaMallocAsync / cudaFreeAsync on `stream`; returns
+ * RA_ERR_ALLOC if that fails.
  */
 ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                         const float* lse, const void* dout, void* dq, void* dk, void* dv,

@@ -1,0 +1,918 @@
+// attn_bwd.cuh -- gradients of the ring-attention forward on tcgen05 tensor
+// cores (sm_103a).
+//
+// The pages describe the forward only; the gradients are the textbook ones of
+// out = softmax(scale q k^T + causal mask) v, recomputing P from the forward's
+// log-sum-exp instead of storing it:
+//   P = exp(scale q k^T - lse),  delta_i = sum_d dout_id out_id,
+//   dv = P^T dout,  dP = dout v^T,  dS = P * (dP - delta),
+//   dq = scale dS k,  dk = scale dS^T q,
+// with dk and dv summed over the H/Hkv query heads that share a key/value head.
+// The causal mask compares global positions ("Zig Zag Ring Attention"), and the
+// key/value blocks meet the query shards in ring order: block s visits shard
+// (s + t) mod P at step t ("Tiefer Einblick": blocks hop from rank to rank).
+//
+// Three kernels:
+//   bwd_prep_kernel       delta and -lse*log2(e) per query row, written in
+//                         tile order (one 128-float slab per 128-slot query
+//                         tile, ragged tails padded so they contribute 0);
+//   attn_bwd_dkdv_kernel  one 128-key tile per work unit; loops over the
+//                         visible query tiles of every head of its group;
+//                         S^T = K Q^T and dP^T = V dO^T into TMEM, P^T and
+//                         dS^T (bf16) back into TMEM, dV += P^T dO and
+//                         dK += dS^T Q accumulated in TMEM;
+//   attn_bwd_dq_kernel    one 128-query tile per work unit; loops over the
+//                         visible key tiles; S = Q K^T, dP = dO V^T, dS (bf16)
+//                         into TMEM, dQ += dS K accumulated in TMEM.
+// dQ is produced by its own pass, so nothing is accumulated with atomics and
+// the result is deterministic; S and dP are computed twice for it.
+//
+// Roles in both tensor-core kernels (384 threads, one persistent CTA per SM):
+//   warp 0       TMA producer,
+//   warp 1       tcgen05 issuer (one thread) and owner of the TMEM allocation,
+//   warps 4..7   "half 0": columns [0, 64) of every S / dP tile,
+//   warps 8..11  "half 1": columns [64, 128).
+// The S / dP products are issued per half (N = 64), so half 0's elementwise
+// work overlaps the tensor core computing half 1, and the accumulating
+// products of one tile overlap the elementwise work of the next.
+//
+// Tensor memory (512 columns): S or S^T [0,128), dP or dP^T [128,256),
+// accumulators from 256 (dK/dV pass: dV [256,256+D), dK [384,384+D);
+// dQ pass: dQ [256,256+D)).  The bf16 P / dS of half x overwrite columns
+// [64x, 64x+32) of their own fp32 region after it has been read.
+#pragma once
+#include "geometry.cuh"
+#include "sm103_ptx.cuh"
+
+namespace ra {
+
+struct BwdParams {
+  Geo g;
+  float scale;         // multiplies dq and dk
+  float scale_log2;    // scale * log2(e)
+  const float* nlse2;  // tile order: -lse * log2(e); padded rows -inf
+  const float* ndelta; // tile order: -delta; padded rows 0
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int64_t num_items;
+};
+
+// Tile-order vectors: slab (b, h, shard, seg, tile) holds 128 floats, one per
+// slot of that query tile.
+__host__ __device__ inline int64_t vec_tile(const Geo& g, int b, int h, int shard, int seg,
+                                            int tile) {
+  return ((((int64_t)b * g.H + h) * g.P + shard) * g.nseg + seg) * g.ntile + tile;
+}
+__host__ __device__ inline int64_t vec_elems(const Geo& g) {
+  return (int64_t)g.B * g.H * g.P * g.nseg * g.ntile * kTile;
+}
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kSubTiles = D / 64;
+  static constexpr int kStages = D == 128 ? 2 : 4;   // streamed tile pairs in flight
+  static constexpr int kVecBytes = kTile * 4;
+};
+
+constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 384;
+
+// TMA coordinates (phase, row) of the tile at offset `off` of the segment
+// starting at position pos0 of shard `shard`, batch b (natural-order tensor).
+__device__ __forceinline__ void bwd_coords(const Geo& g, int shard, int pos0, int off, int b,
+                                           int& phase, int& row) {
+  if (g.layout == LAYOUT_STRIPED) {
+    phase = shard;
+    row = b * g.n + off;
+  } else {
+    phase = 0;
+    row = b * g.S + pos0 + off;
+  }
+}
+
+// ---------------------------------------------------------------- prep
+// delta = rowsum(dout * out) and -lse * log2(e) for every query row, in tile
+// order.  D/8 lanes share a row (16 bytes of dout and of out each).
+template <int D>
+__global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ out,
+                                const __nv_bfloat16* __restrict__ dout,
+                                const float* __restrict__ lse, float* __restrict__ nlse2,
+                                float* __restrict__ ndelta, Geo g) {
+  constexpr int kLanes = D / 8;
+  constexpr int kRowsPerWarp = 32 / kLanes;
+  const int lane = threadIdx.x % 32;
+  const int sub = lane / kLanes, piece = lane % kLanes;
+  const int64_t rows = vec_elems(g);
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  for (int64_t base = warp0 * kRowsPerWarp; base < rows; base += warps_total * kRowsPerWarp) {
+    const int64_t e = base + sub;
+    float acc = 0.f;
+    bool real = false;
+    int64_t lidx = 0;
+    if (e < rows) {
+      int64_t t = e / kTile;
+      const int i = (int)(e % kTile);
+      const int tile = (int)(t % g.ntile); t /= g.ntile;
+      const int seg = (int)(t % g.nseg); t /= g.nseg;
+      const int shard = (int)(t % g.P); t /= g.P;
+      const int h = (int)(t % g.H);
+      const int b = (int)(t / g.H);
+      const QTile qt = make_qtile(g, shard, seg, tile);
+      if (i < qt.valid) {
+        real = true;
+        const int64_t pos = qt.pos0 + (int64_t)qt.stride * (qt.off + i);
+        const int64_t off = (((int64_t)b * g.S + pos) * g.H + h) * D + piece * 8;
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(out + off));
+        const uint4 c = __ldg(reinterpret_cast<const uint4*>(dout + off));
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[j]));
+          const float2 fc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cv[j]));
+          acc = fmaf(fa.x, fc.x, acc);
+          acc = fmaf(fa.y, fc.y, acc);
+        }
+        lidx = ((int64_t)b * g.H + h) * g.S + pos;
+      }
+    }
+#pragma unroll
+    for (int o = kLanes / 2; o > 0; o /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (e < rows && piece == 0) {
+      ndelta[e] = real ? -acc : 0.f;
+      nlse2[e] = real ? -__ldg(lse + lidx) * 1.4426950408889634f : -INFINITY;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- schedule
+// dK/dV pass: work item -> (b, kv head, key tile).  Within a (b, kv head) the
+// key tiles come in increasing position, so under a causal mask the tiles
+// that see the most queries come first.
+struct KUnit {
+  int b, hkv, shard, seg, tile;
+};
+
+__device__ __forceinline__ KUnit kunit_of(const Geo& g, int64_t item) {
+  const int64_t U = (int64_t)g.P * g.nseg * g.ntile;
+  const int64_t bg = item / U;
+  const int64_t u = item % U;
+  KUnit w;
+  w.b = (int)(bg / g.Hkv);
+  w.hkv = (int)(bg % g.Hkv);
+  if (g.layout == LAYOUT_STRIPED) {
+    w.tile = (int)(u / g.P);
+    w.shard = (int)(u % g.P);
+    w.seg = 0;
+  } else if (g.layout == LAYOUT_ZIGZAG) {
+    const int chunk = (int)(u / g.ntile);
+    w.tile = (int)(u % g.ntile);
+    if (chunk < g.P) { w.shard = chunk; w.seg = 0; }
+    else { w.shard = 2 * g.P - 1 - chunk; w.seg = 1; }
+  } else {
+    w.shard = (int)(u / g.ntile);
+    w.tile = (int)(u % g.ntile);
+    w.seg = 0;
+  }
+  return w;
+}
+
+// dQ pass: work item -> (b, h, query tile), decreasing position within (b, h).
+struct QUnit {
+  int b, h, shard, seg, tile;
+};
+
+__device__ __forceinline__ QUnit qunit_of(const Geo& g, int64_t item) {
+  const int64_t U = (int64_t)g.P * g.nseg * g.ntile;
+  const int64_t bh = item / U;
+  const int64_t u = item % U;
+  QUnit w;
+  w.b = (int)(bh / g.H);
+  w.h = (int)(bh % g.H);
+  if (g.layout == LAYOUT_STRIPED) {
+    w.tile = g.ntile - 1 - (int)(u / g.P);
+    w.shard = g.P - 1 - (int)(u % g.P);
+    w.seg = 0;
+  } else if (g.layout == LAYOUT_ZIGZAG) {
+    const int chunk = 2 * g.P - 1 - (int)(u / g.ntile);
+    w.tile = g.ntile - 1 - (int)(u % g.ntile);
+    if (chunk < g.P) { w.shard = chunk; w.seg = 0; }
+    else { w.shard = 2 * g.P - 1 - chunk; w.seg = 1; }
+  } else {
+    w.shard = g.P - 1 - (int)(u / g.ntile);
+    w.tile = g.ntile - 1 - (int)(u % g.ntile);
+    w.seg = 0;
+  }
+  return w;
+}
+
+// Query tiles a key tile meets, in ring order: for each query head of the
+// group, steps t = 0..P-1 visit shard r = (s + t) mod P; in each segment of r
+// the tiles holding a position >= kmin (all tiles without a causal mask) are a
+// suffix [a, ntile).
+struct QIter {
+  int e, t, sq, a, a_end;
+  int r, h, hkv, s, kmin;
+  Seg seg;
+};
+
+__device__ __forceinline__ void qiter_range(const Geo& g, QIter& it) {
+  it.seg = segment_of(g, it.r, it.sq);
+  const int first = g.causal ? count_le(it.seg, it.kmin - 1) : 0;
+  if (first >= it.seg.len) {
+    it.a = 0;
+    it.a_end = 0;
+  } else {
+    it.a = first / kTile;
+    it.a_end = g.ntile;
+  }
+}
+
+__device__ __forceinline__ void qiter_setup(const Geo& g, QIter& it, int hkv, int s, int kmin) {
+  it.e = 0; it.t = 0; it.sq = 0;
+  it.hkv = hkv; it.s = s; it.kmin = kmin;
+  it.h = hkv * (g.H / g.Hkv);
+  it.r = s;
+  qiter_range(g, it);
+}
+
+__device__ __forceinline__ bool qiter_next(const Geo& g, QIter& it) {
+  while (it.a >= it.a_end) {
+    if (++it.sq >= g.nseg) {
+      it.sq = 0;
+      if (++it.t >= g.P) {
+        it.t = 0;
+        if (++it.e >= g.H / g.Hkv) return false;
+        it.h = it.hkv * (g.H / g.Hkv) + it.e;
+      }
+      it.r = (it.s + it.t) % g.P;
+    }
+    qiter_range(g, it);
+  }
+  return true;
+}
+
+// Key tiles a query tile meets, in ring order s = (r - t) mod P; the visible
+// tiles of each key segment are a prefix (positions <= qmax).
+struct KIterB {
+  int t, sk, bt, nk, s, r, qmax;
+  Seg seg;
+};
+
+__device__ __forceinline__ void kiterb_setup(const Geo& g, KIterB& it, int r, int qmax) {
+  it.t = 0; it.sk = 0; it.bt = 0; it.r = r; it.qmax = qmax;
+  it.s = r;
+  it.seg = segment_of(g, it.s, 0);
+  it.nk = visible_tiles(g, it.seg, qmax);
+}
+
+__device__ __forceinline__ bool kiterb_next(const Geo& g, KIterB& it) {
+  while (it.bt >= it.nk) {
+    it.bt = 0;
+    if (++it.sk >= g.nseg) {
+      it.sk = 0;
+      if (++it.t >= g.P) return false;
+      it.s = ring_block(g, it.r, it.t);
+    }
+    it.seg = segment_of(g, it.s, it.sk);
+    it.nk = visible_tiles(g, it.seg, it.qmax);
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- shared memory
+template <int D>
+struct __align__(1024) DkdvSmem {
+  uint8_t k[BwdCfg<D>::kTileBytes];
+  uint8_t v[BwdCfg<D>::kTileBytes];
+  uint8_t q[BwdCfg<D>::kStages][BwdCfg<D>::kTileBytes];
+  uint8_t dO[BwdCfg<D>::kStages][BwdCfg<D>::kTileBytes];
+  float nlse2[BwdCfg<D>::kStages][kTile];
+  float ndelta[BwdCfg<D>::kStages][kTile];
+  uint64_t kv_full, kv_empty;
+  uint64_t st_full[BwdCfg<D>::kStages], st_empty[BwdCfg<D>::kStages];
+  uint64_t s_full[2], p_full[2];
+  uint64_t acc_full, acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+struct __align__(1024) DqSmem {
+  uint8_t q[BwdCfg<D>::kTileBytes];
+  uint8_t dO[BwdCfg<D>::kTileBytes];
+  uint8_t k[BwdCfg<D>::kStages][BwdCfg<D>::kTileBytes];
+  uint8_t v[BwdCfg<D>::kStages][BwdCfg<D>::kTileBytes];
+  uint64_t q_full, q_empty;
+  uint64_t st_full[BwdCfg<D>::kStages], st_empty[BwdCfg<D>::kStages];
+  uint64_t s_full[2], p_full[2];
+  uint64_t acc_full, acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// S_x (or S^T_x) = A B_x^T over the D contraction, N = 64 rows of B starting
+// at row 64x; both operands K-major (128-byte swizzle, D/64 sub-tiles).
+template <int D>
+__device__ __forceinline__ void issue_half_product(uint32_t d_tmem, uint32_t a_base,
+                                                   uint32_t b_base, int x) {
+  constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
+    mma_ss(d_tmem, sdesc_sw128(a_base + off, 16, 1024),
+           sdesc_sw128(b_base + x * (64 * 128) + off, 16, 1024), id, kk > 0 ? 1u : 0u);
+  }
+}
+
+// acc += A_x B[64x .. 64x+64, :] with A_x (bf16, 128 lanes x 64 values) in
+// TMEM and B a 128 x D tile in shared memory read MN-major.
+template <int D>
+__device__ __forceinline__ void issue_half_accumulate(uint32_t acc_tmem, uint32_t a_tmem,
+                                                      uint32_t b_base, int x, bool first) {
+  constexpr uint32_t id = idesc_bf16(128, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_ts(acc_tmem, a_tmem + kk * 8,
+           sdesc_sw128(b_base + (4 * x + kk) * 2048, kTile * 128, 1024), id,
+           (first && kk == 0) ? 0u : 1u);
+}
+
+// Stores 32 fp32 accumulator columns of one row as bf16, times `mul`.
+__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint32_t (&r)[32],
+                                                 float mul) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d4[i] = make_uint4(
+        pack_bf16x2(__uint_as_float(r[8 * i + 0]) * mul, __uint_as_float(r[8 * i + 1]) * mul),
+        pack_bf16x2(__uint_as_float(r[8 * i + 2]) * mul, __uint_as_float(r[8 * i + 3]) * mul),
+        pack_bf16x2(__uint_as_float(r[8 * i + 4]) * mul, __uint_as_float(r[8 * i + 5]) * mul),
+        pack_bf16x2(__uint_as_float(r[8 * i + 6]) * mul, __uint_as_float(r[8 * i + 7]) * mul));
+}
+
+// ---------------------------------------------------------------- dK / dV pass
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  constexpr int kSt = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  DkdvSmem<D>& sm = *reinterpret_cast<DkdvSmem<D>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid / 32, lane = tid % 32;
+  volatile int* abort_flag = &sm.abort_flag;
+  const Geo& g = p.g;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&sm.kv_full), 1);
+    mbar_init(smem_u32(&sm.kv_empty), 1);
+    for (int i = 0; i < kSt; ++i) {
+      mbar_init(smem_u32(&sm.st_full[i]), 1);
+      mbar_init(smem_u32(&sm.st_empty[i]), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&sm.s_full[x]), 1);
+      mbar_init(smem_u32(&sm.p_full[x]), 128);
+    }
+    mbar_init(smem_u32(&sm.acc_full), 1);
+    mbar_init(smem_u32(&sm.acc_empty), 256);
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  const int64_t G = gridDim.x;
+  const int64_t c = blockIdx.x;
+  auto item_at = [&](int64_t k) -> int64_t { return k * G + ((k & 1) ? (G - 1 - c) : c); };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      const uint64_t pol_kv = policy_evict_first();
+      const uint64_t pol_q = policy_evict_last();
+      uint32_t kv_ph = 0, st = 0, st_ph = 0;
+      for (int64_t k = 0;; ++k) {
+        const int64_t item = item_at(k);
+        if (item >= p.num_items) break;
+        const KUnit w = kunit_of(g, item);
+        const QTile kt = make_qtile(g, w.shard, w.seg, w.tile);
+        QIter it;
+        qiter_setup(g, it, w.hkv, w.shard, kt.qmin);
+        if (!kt.valid || !qiter_next(g, it)) continue;
+        if (!mbar_wait(smem_u32(&sm.kv_empty), kv_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag)) goto done;
+        kv_ph ^= 1;
+        {
+          const uint32_t bar = smem_u32(&sm.kv_full);
+          mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
+          int phase, row;
+          bwd_coords(g, w.shard, kt.pos0, kt.off, w.b, phase, row);
+#pragma unroll
+          for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
+            tma_load_4d(smem_u32(sm.k) + s2 * (kTile * 128), &tm_k, bar, 64 * s2, w.hkv, phase,
+                        row, pol_kv);
+            tma_load_4d(smem_u32(sm.v) + s2 * (kTile * 128), &tm_v, bar, 64 * s2, w.hkv, phase,
+                        row, pol_kv);
+          }
+        }
+        do {
+          if (!mbar_wait(smem_u32(&sm.st_empty[st]), st_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
+            goto done;
+          const uint32_t bar = smem_u32(&sm.st_full[st]);
+          mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes + 2 * Cfg::kVecBytes);
+          int phase, row;
+          bwd_coords(g, it.r, it.seg.pos0, it.a * kTile, w.b, phase, row);
+#pragma unroll
+          for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
+            tma_load_4d(smem_u32(sm.q[st]) + s2 * (kTile * 128), &tm_q, bar, 64 * s2, it.h, phase,
+                        row, pol_q);
+            tma_load_4d(smem_u32(sm.dO[st]) + s2 * (kTile * 128), &tm_do, bar, 64 * s2, it.h,
+                        phase, row, pol_q);
+          }
+          const int64_t vt = vec_tile(g, w.b, it.h, it.r, it.sq, it.a) * kTile;
+          bulk_load(smem_u32(sm.nlse2[st]), p.nlse2 + vt, Cfg::kVecBytes, bar, pol_q);
+          bulk_load(smem_u32(sm.ndelta[st]), p.ndelta + vt, Cfg::kVecBytes, bar, pol_q);
+          if (++st == kSt) { st = 0; st_ph ^= 1; }
+          ++it.a;
+        } while (qiter_next(g, it));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      uint32_t kv_ph = 0, st = 0, st_ph = 0, p_ph0 = 0, p_ph1 = 0, acc_ph = 0;
+      const uint32_t kb = smem_u32(sm.k), vb = smem_u32(sm.v);
+      for (int64_t k = 0;; ++k) {
+        const int64_t item = item_at(k);
+        if (item >= p.num_items) break;
+        const KUnit w = kunit_of(g, item);
+        const QTile kt = make_qtile(g, w.shard, w.seg, w.tile);
+        QIter it;
+        qiter_setup(g, it, w.hkv, w.shard, kt.qmin);
+        if (!kt.valid || !qiter_next(g, it)) continue;
+        if (!mbar_wait(smem_u32(&sm.kv_full), kv_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
+        kv_ph ^= 1;
+        if (!mbar_wait(smem_u32(&sm.st_full[st]), st_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
+        tc_fence_after();
+        // S^T_x = K Q_x^T and dP^T_x = V dO_x^T for both halves of the first tile
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          issue_half_product<D>(tmem + kColS + 64 * x, kb, smem_u32(sm.q[st]), x);
+          issue_half_product<D>(tmem + kColDP + 64 * x, vb, smem_u32(sm.dO[st]), x);
+          mma_commit(smem_u32(&sm.s_full[x]));
+        }
+        bool first = true;
+        for (;;) {
+          const uint32_t cur = st;
+          ++it.a;
+          const bool more = qiter_next(g, it);
+          uint32_t nst = st + 1, nph = st_ph;
+          if (nst == (uint32_t)kSt) { nst = 0; nph ^= 1; }
+          // half 0: dV += P^T_0 dO_0, dK += dS^T_0 Q_0
+          if (!mbar_wait(smem_u32(&sm.p_full[0]), p_ph0, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
+          p_ph0 ^= 1;
+          tc_fence_after();
+          if (first) {
+            if (!mbar_wait(smem_u32(&sm.acc_empty), acc_ph ^ 1, RA_DEV_TIMEOUT_MMA, abort_flag))
+              goto done;
+            tc_fence_after();
+          }
+          issue_half_accumulate<D>(tmem + kColAcc0, tmem + kColS, smem_u32(sm.dO[cur]), 0, first);
+          issue_half_accumulate<D>(tmem + kColAcc1, tmem + kColDP, smem_u32(sm.q[cur]), 0, first);
+          if (more) {
+            if (!mbar_wait(smem_u32(&sm.st_full[nst]), nph, RA_DEV_TIMEOUT_MMA, abort_flag))
+              goto done;
+            tc_fence_after();
+            issue_half_product<D>(tmem + kColS, kb, smem_u32(sm.q[nst]), 0);
+            issue_half_product<D>(tmem + kColDP, vb, smem_u32(sm.dO[nst]), 0);
+            mma_commit(smem_u32(&sm.s_full[0]));
+          }
+          // half 1
+          if (!mbar_wait(smem_u32(&sm.p_full[1]), p_ph1, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
+          p_ph1 ^= 1;
+          tc_fence_after();
+          issue_half_accumulate<D>(tmem + kColAcc0, tmem + kColS + 64, smem_u32(sm.dO[cur]), 1,
+                                   false);
+          issue_half_accumulate<D>(tmem + kColAcc1, tmem + kColDP + 64, smem_u32(sm.q[cur]), 1,
+                                   false);
+          mma_commit(smem_u32(&sm.st_empty[cur]));
+          st = nst;
+          st_ph = nph;
+          first = false;
+          if (!more) break;
+          issue_half_product<D>(tmem + kColS + 64, kb, smem_u32(sm.q[st]), 1);
+          issue_half_product<D>(tmem + kColDP + 64, vb, smem_u32(sm.dO[st]), 1);
+          mma_commit(smem_u32(&sm.s_full[1]));
+        }
+        mma_commit(smem_u32(&sm.acc_full));
+        mma_commit(smem_u32(&sm.kv_empty));
+        acc_ph ^= 1;
+      }
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- elementwise halves
+    const int x = (warp - 4) / 4;                 // column half of S^T / dP^T
+    const int quarter = warp % 4;                 // TMEM lanes [32*quarter, +32)
+    const int row = quarter * 32 + lane;          // key row of the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_addr + kColS + 64 * x;
+    const uint32_t t_dp = tmem + lane_addr + kColDP + 64 * x;
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    uint32_t s_ph = 0, st = 0, st_ph = 0, acc_ph = 0;
+    for (int64_t k = 0;; ++k) {
+      const int64_t item = item_at(k);
+      if (item >= p.num_items) break;
+      const KUnit w = kunit_of(g, item);
+      const QTile kt = make_qtile(g, w.shard, w.seg, w.tile);
+      QIter it;
+      qiter_setup(g, it, w.hkv, w.shard, kt.qmin);
+      if (!kt.valid || !qiter_next(g, it)) continue;
+      const int kpos = kt.pos0 + kt.stride * (kt.off + row);
+      do {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[x]), s_ph,
+                                               RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
+          goto done;
+        s_ph ^= 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.st_full[st]), st_ph,
+                                               RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
+          goto done;
+        tc_fence_after();
+        const QTile qt = make_qtile(g, it.r, it.sq, it.a);
+        // query columns below `lo` precede this key: masked out
+        int lo = 0;
+        if (g.causal && qt.qmin < kt.qmax) {
+          const int cnt = count_le(it.seg, kpos - 1) - qt.off;
+          lo = cnt < 0 ? 0 : (cnt > kTile ? kTile : cnt);
+        }
+        const float* nl = sm.nlse2[st] + 64 * x;
+        const float* nd = sm.ndelta[st] + 64 * x;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t s[32], dp[32];
+          tmem_ld32(t_s + 32 * c2, s);
+          tmem_ld32(t_dp + 32 * c2, dp);
+          tmem_wait_ld();
+          uint32_t pk_p[16], pk_ds[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 nl4 = *reinterpret_cast<const float4*>(nl + 32 * c2 + i);
+            const float4 nd4 = *reinterpret_cast<const float4*>(nd + 32 * c2 + i);
+#pragma unroll
+            for (int j = 0; j < 4; j += 2) {
+              const int qc = 64 * x + 32 * c2 + i + j;   // query column within the tile
+              const float2 nlj = j == 0 ? make_float2(nl4.x, nl4.y) : make_float2(nl4.z, nl4.w);
+              const float2 ndj = j == 0 ? make_float2(nd4.x, nd4.y) : make_float2(nd4.z, nd4.w);
+              const float2 t2 = fma2(make_float2(__uint_as_float(s[i + j]),
+                                                 __uint_as_float(s[i + j + 1])), sl2, nlj);
+              float p0 = ex2_approx(t2.x), p1 = ex2_approx(t2.y);
+              p0 = qc < lo ? 0.f : p0;
+              p1 = qc + 1 < lo ? 0.f : p1;
+              const float2 dd = add2(make_float2(__uint_as_float(dp[i + j]),
+                                                 __uint_as_float(dp[i + j + 1])), ndj);
+              const float2 ds = mul2(make_float2(p0, p1), dd);
+              pk_p[(i + j) / 2] = pack_bf16x2(p0, p1);
+              pk_ds[(i + j) / 2] = pack_bf16x2(ds.x, ds.y);
+            }
+          }
+          tmem_st16(t_s + 16 * c2, pk_p);
+          tmem_st16(t_dp + 16 * c2, pk_ds);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.p_full[x]));
+        if (++st == (uint32_t)kSt) { st = 0; st_ph ^= 1; }
+        ++it.a;
+      } while (qiter_next(g, it));
+      // ---- epilogue: half 0 stores dV, half 1 stores scale * dK
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_full), acc_ph,
+                                             RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
+        goto done;
+      acc_ph ^= 1;
+      tc_fence_after();
+      {
+        __nv_bfloat16* dst = x == 0 ? p.dv : p.dk;
+        const float mul = x == 0 ? 1.f : p.scale;
+        const uint32_t t_acc = tmem + lane_addr + (x == 0 ? kColAcc0 : kColAcc1);
+        const int64_t orow = ((int64_t)w.b * g.S + kpos) * g.Hkv + w.hkv;
+#pragma unroll
+        for (int cch = 0; cch < D / 32; ++cch) {
+          uint32_t r[32];
+          tmem_ld32(t_acc + 32 * cch, r);
+          tmem_wait_ld();
+          if (row < kt.valid) store_row32_bf16(dst + orow * D + 32 * cch, r, mul);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.acc_empty));
+    }
+  }
+
+done:
+  tc_fence_before();
+  __syncthreads();
+  if (sm.abort_flag) {
+    if (warp == 1 && lane == 0) {
+      mma_commit(smem_u32(&sm.drain));
+      mbar_wait(smem_u32(&sm.drain), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
+    }
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 1000000ull) {
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- dQ pass
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  constexpr int kSt = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  DqSmem<D>& sm = *reinterpret_cast<DqSmem<D>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid / 32, lane = tid % 32;
+  volatile int* abort_flag = &sm.abort_flag;
+  const Geo& g = p.g;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&sm.q_full), 1);
+    mbar_init(smem_u32(&sm.q_empty), 1);
+    for (int i = 0; i < kSt; ++i) {
+      mbar_init(smem_u32(&sm.st_full[i]), 1);
+      mbar_init(smem_u32(&sm.st_empty[i]), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&sm.s_full[x]), 1);
+      mbar_init(smem_u32(&sm.p_full[x]), 128);
+    }
+    mbar_init(smem_u32(&sm.acc_full), 1);
+    mbar_init(smem_u32(&sm.acc_empty), 256);
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  const int64_t G = gridDim.x;
+  const int64_t c = blockIdx.x;
+  auto item_at = [&](int64_t k) -> int64_t { return k * G + ((k & 1) ? (G - 1 - c) : c); };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      uint32_t q_ph = 0, st = 0, st_ph = 0;
+      for (int64_t k = 0;; ++k) {
+        const int64_t item = item_at(k);
+        if (item >= p.num_items) break;
+        const QUnit w = qunit_of(g, item);
+        const QTile qt = make_qtile(g, w.shard, w.seg, w.tile);
+        if (!qt.valid) continue;
+        KIterB it;
+        kiterb_setup(g, it, w.shard, qt.qmax);
+        if (!kiterb_next(g, it)) continue;
+        if (!mbar_wait(smem_u32(&sm.q_empty), q_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag)) goto done;
+        q_ph ^= 1;
+        {
+          const uint32_t bar = smem_u32(&sm.q_full);
+          mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
+          int phase, row;
+          bwd_coords(g, w.shard, qt.pos0, qt.off, w.b, phase, row);
+#pragma unroll
+          for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
+            tma_load_4d(smem_u32(sm.q) + s2 * (kTile * 128), &tm_q, bar, 64 * s2, w.h, phase, row,
+                        pol_q);
+            tma_load_4d(smem_u32(sm.dO) + s2 * (kTile * 128), &tm_do, bar, 64 * s2, w.h, phase,
+                        row, pol_q);
+          }
+        }
+        const int hkv = w.h / (g.H / g.Hkv);
+        do {
+          if (!mbar_wait(smem_u32(&sm.st_empty[st]), st_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
+            goto done;
+          const uint32_t bar = smem_u32(&sm.st_full[st]);
+          mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
+          int phase, row;
+          bwd_coords(g, it.s, it.seg.pos0, it.bt * kTile, w.b, phase, row);
+#pragma unroll
+          for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
+            tma_load_4d(smem_u32(sm.k[st]) + s2 * (kTile * 128), &tm_k, bar, 64 * s2, hkv, phase,
+                        row, pol_kv);
+            tma_load_4d(smem_u32(sm.v[st]) + s2 * (kTile * 128), &tm_v, bar, 64 * s2, hkv, phase,
+                        row, pol_kv);
+          }
+          if (++st == kSt) { st = 0; st_ph ^= 1; }
+          ++it.bt;
+        } while (kiterb_next(g, it));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      uint32_t q_ph = 0, st = 0, st_ph = 0, p_ph0 = 0, p_ph1 = 0, acc_ph = 0;
+      const uint32_t qb = smem_u32(sm.q), dob = smem_u32(sm.dO);
+      for (int64_t k = 0;; ++k) {
+        const int64_t item = item_at(k);
+        if (item >= p.num_items) break;
+        const QUnit w = qunit_of(g, item);
+        const QTile qt = make_qtile(g, w.shard, w.seg, w.tile);
+        if (!qt.valid) continue;
+        KIterB it;
+        kiterb_setup(g, it, w.shard, qt.qmax);
+        if (!kiterb_next(g, it)) continue;
+        if (!mbar_wait(smem_u32(&sm.q_full), q_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
+        q_ph ^= 1;
+        if (!mbar_wait(smem_u32(&sm.st_full[st]), st_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
+        tc_fence_after();
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          issue_half_product<D>(tmem + kColS + 64 * x, qb, smem_u32(sm.k[st]), x);
+          issue_half_product<D>(tmem + kColDP + 64 * x, dob, smem_u32(sm.v[st]), x);
+          mma_commit(smem_u32(&sm.s_full[x]));
+        }
+        bool first = true;
+        for (;;) {
+          const uint32_t cur = st;
+          ++it.bt;
+          const bool more = kiterb_next(g, it);
+          uint32_t nst = st + 1, nph = st_ph;
+          if (nst == (uint32_t)kSt) { nst = 0; nph ^= 1; }
+          // dQ += dS_0 K[0:64]
+          if (!mbar_wait(smem_u32(&sm.p_full[0]), p_ph0, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
+          p_ph0 ^= 1;
+          tc_fence_after();
+          if (first) {
+            if (!mbar_wait(smem_u32(&sm.acc_empty), acc_ph ^ 1, RA_DEV_TIMEOUT_MMA, abort_flag))
+              goto done;
+            tc_fence_after();
+          }
+          issue_half_accumulate<D>(tmem + kColAcc0, tmem + kColS, smem_u32(sm.k[cur]), 0, first);
+          if (more) {
+            if (!mbar_wait(smem_u32(&sm.st_full[nst]), nph, RA_DEV_TIMEOUT_MMA, abort_flag))
+              goto done;
+            tc_fence_after();
+            issue_half_product<D>(tmem + kColS, qb, smem_u32(sm.k[nst]), 0);
+            issue_half_product<D>(tmem + kColDP, dob, smem_u32(sm.v[nst]), 0);
+            mma_commit(smem_u32(&sm.s_full[0]));
+          }
+          // dQ += dS_1 K[64:128]
+          if (!mbar_wait(smem_u32(&sm.p_full[1]), p_ph1, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
+          p_ph1 ^= 1;
+          tc_fence_after();
+          issue_half_accumulate<D>(tmem + kColAcc0, tmem + kColS + 64, smem_u32(sm.k[cur]), 1,
+                                   false);
+          mma_commit(smem_u32(&sm.st_empty[cur]));
+          st = nst;
+          st_ph = nph;
+          first = false;
+          if (!more) break;
+          issue_half_product<D>(tmem + kColS + 64, qb, smem_u32(sm.k[st]), 1);
+          issue_half_product<D>(tmem + kColDP + 64, dob, smem_u32(sm.v[st]), 1);
+          mma_commit(smem_u32(&sm.s_full[1]));
+        }
+        mma_commit(smem_u32(&sm.acc_full));
+        mma_commit(smem_u32(&sm.q_empty));
+        acc_ph ^= 1;
+      }
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- elementwise halves
+    const int x = (warp - 4) / 4;                 // key-column half of S / dP
+    const int quarter = warp % 4;
+    const int row = quarter * 32 + lane;          // query row of the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_addr + kColS + 64 * x;
+    const uint32_t t_dp = tmem + lane_addr + kColDP + 64 * x;
+    const float sl2 = p.scale_log2;
+    uint32_t s_ph = 0, acc_ph = 0;
+    for (int64_t k = 0;; ++k) {
+      const int64_t item = item_at(k);
+      if (item >= p.num_items) break;
+      const QUnit w = qunit_of(g, item);
+      const QTile qt = make_qtile(g, w.shard, w.seg, w.tile);
+      if (!qt.valid) continue;
+      KIterB it;
+      kiterb_setup(g, it, w.shard, qt.qmax);
+      if (!kiterb_next(g, it)) continue;
+      const int qpos = qt.pos0 + qt.stride * (qt.off + row);
+      const int64_t vi = vec_tile(g, w.b, w.h, w.shard, w.seg, w.tile) * kTile + row;
+      const float nl = __ldg(p.nlse2 + vi);
+      const float nd = __ldg(p.ndelta + vi);
+      const float2 sl2_2 = make_float2(sl2, sl2), nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
+      do {
+        const int k0 = it.bt * kTile;
+        const int kleft = it.seg.len - k0;
+        const int kvalid = kleft < kTile ? kleft : kTile;
+        int lim = kvalid;   // key columns at or beyond `lim` are masked out
+        if (g.causal && it.seg.pos0 + it.seg.stride * (k0 + kvalid - 1) > qt.qmin) {
+          const int cl = count_le(it.seg, qpos) - k0;
+          lim = cl < 0 ? 0 : (cl > kvalid ? kvalid : cl);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[x]), s_ph,
+                                               RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
+          goto done;
+        s_ph ^= 1;
+        tc_fence_after();
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t s[32], dp[32];
+          tmem_ld32(t_s + 32 * c2, s);
+          tmem_ld32(t_dp + 32 * c2, dp);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int kc = 64 * x + 32 * c2 + i;   // key column within the tile
+            const float2 t2 = fma2(make_float2(__uint_as_float(s[i]), __uint_as_float(s[i + 1])),
+                                   sl2_2, nl2);
+            float p0 = ex2_approx(t2.x), p1 = ex2_approx(t2.y);
+            p0 = kc < lim ? p0 : 0.f;
+            p1 = kc + 1 < lim ? p1 : 0.f;
+            const float2 dd = add2(make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])),
+                                   nd2);
+            const float2 ds = mul2(make_float2(p0, p1), dd);
+            pk[i / 2] = pack_bf16x2(ds.x, ds.y);
+          }
+          tmem_st16(t_s + 16 * c2, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.p_full[x]));
+        ++it.bt;
+      } while (kiterb_next(g, it));
+      // ---- epilogue: half x stores dq columns [x*D/2, (x+1)*D/2), times scale
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_full), acc_ph,
+                                             RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
+        goto done;
+      acc_ph ^= 1;
+      tc_fence_after();
+      {
+        const uint32_t t_acc = tmem + lane_addr + kColAcc0 + x * (D / 2);
+        const int64_t orow = ((int64_t)w.b * g.S + qpos) * g.H + w.h;
+#pragma unroll
+        for (int cch = 0; cch < D / 64; ++cch) {
+          uint32_t r[32];
+          tmem_ld32(t_acc + 32 * cch, r);
+          tmem_wait_ld();
+          if (row < qt.valid) store_row32_bf16(p.dq + orow * D + x * (D / 2) + 32 * cch, r, p.scale);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.acc_empty));
+    }
+  }
+
+done:
+  tc_fence_before();
+  __syncthreads();
+  if (sm.abort_flag) {
+    if (warp == 1 && lane == 0) {
+      mma_commit(smem_u32(&sm.drain));
+      mbar_wait(smem_u32(&sm.drain), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
+    }
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 1000000ull) {
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace ra

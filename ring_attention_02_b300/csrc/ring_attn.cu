@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "../../include/ring_attn.h"
+#include "attn_bwd.cuh"
 #include "attn_fwd.cuh"
 #include "elementwise.cuh"
 #include "geometry.cuh"
@@ -204,6 +205,104 @@ ra_status fwd_impl(int mode, const void* q, const void* k, const void* v, void* 
                   : launch_fwd_d<64>(mq, mk, mv, prm, dev, stream);
 }
 
+struct BwdArgs {
+  const void *q, *k, *v, *out;
+  const float* lse;
+  const void* dout;
+  void *dq, *dk, *dv;
+  int B, H, Hkv;
+  int64_t S;
+  int D, P, layout, causal;
+  float scale;
+};
+
+ra_status check_bwd(const BwdArgs& a) {
+  if (!a.q || !a.k || !a.v || !a.out || !a.lse || !a.dout || !a.dq || !a.dk || !a.dv)
+    return fail(RA_ERR_NULL, "q, k, v, out, lse, dout, dq, dk and dv must be non-NULL");
+  ra_status st = check_common(a.B, a.H, a.Hkv, a.S, a.D, a.P, a.layout, a.scale);
+  if (st != RA_OK) return st;
+  const void* p16[] = {a.q, a.k, a.v, a.out, a.dout, a.dq, a.dk, a.dv};
+  for (const void* ptr : p16)
+    if (!aligned16(ptr)) return fail(RA_ERR_ALIGN, "q, k, v, out, dout, dq, dk, dv must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(a.lse) & 3u) return fail(RA_ERR_ALIGN, "lse must be 4-byte aligned");
+  return RA_OK;
+}
+
+template <int D>
+ra_status launch_bwd_d(const BwdArgs& a, float* nlse2, float* ndelta, DeviceInfo* dev,
+                       cudaStream_t stream) {
+  const size_t smem_kv = sizeof(ra::DkdvSmem<D>) + 1024;
+  const size_t smem_q = sizeof(ra::DqSmem<D>) + 1024;
+  const int di = D == 128 ? 1 : 0;
+  if (!dev->bwd_attr_set[di]) {
+    cudaError_t e = cudaFuncSetAttribute(ra::attn_bwd_dkdv_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dkdv smem)");
+    e = cudaFuncSetAttribute(ra::attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_q);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dq smem)");
+    dev->bwd_attr_set[di] = true;
+  }
+  ra::BwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.g = ra::make_geo(a.B, a.H, a.Hkv, a.S, a.P, a.layout, a.causal ? 1 : 0);
+  prm.scale = a.scale;
+  prm.scale_log2 = a.scale * 1.4426950408889634f;
+  prm.nlse2 = nlse2;
+  prm.ndelta = ndelta;
+  prm.dq = static_cast<__nv_bfloat16*>(a.dq);
+  prm.dk = static_cast<__nv_bfloat16*>(a.dk);
+  prm.dv = static_cast<__nv_bfloat16*>(a.dv);
+  const ra::Geo& g = prm.g;
+
+  CUtensorMap mq, mk, mv, mdo;
+  const int64_t n = a.S / a.P;
+  const bool striped = a.layout == RA_LAYOUT_STRIPED;
+  const int64_t phases = striped ? a.P : 1;
+  const int64_t rows = striped ? (int64_t)a.B * n : (int64_t)a.B * a.S;
+  ra_status st = make_token_map(&mq, a.q, D, a.H, phases, rows);
+  if (st == RA_OK) st = make_token_map(&mk, a.k, D, a.Hkv, phases, rows);
+  if (st == RA_OK) st = make_token_map(&mv, a.v, D, a.Hkv, phases, rows);
+  if (st == RA_OK) st = make_token_map(&mdo, a.dout, D, a.H, phases, rows);
+  if (st != RA_OK) return st;
+
+  // delta and -lse*log2(e) in tile order
+  const int64_t vrows = ra::vec_elems(g);
+  const int rows_per_block = 8 * (32 / (D / 8));
+  int64_t blocks = (vrows + rows_per_block - 1) / rows_per_block;
+  const int64_t cap = (int64_t)dev->sms * 8;
+  if (blocks > cap) blocks = cap;
+  ra::bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
+      nlse2, ndelta, g);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bwd_prep_kernel launch");
+
+  const int64_t units = (int64_t)g.P * g.nseg * g.ntile;
+  prm.num_items = units * a.B * a.Hkv;
+  int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  ra::attn_bwd_dkdv_kernel<D><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dkdv_kernel launch");
+
+  prm.num_items = units * a.B * a.H;
+  grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  ra::attn_bwd_dq_kernel<D><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dq_kernel launch");
+  return RA_OK;
+}
+
+// Launches the three backward kernels on `stream` with caller-provided
+// workspace: nlse2 and ndelta each hold vec_elems(geometry) floats.
+ra_status bwd_launch(const BwdArgs& a, float* nlse2, float* ndelta, cudaStream_t stream) {
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  return a.D == 128 ? launch_bwd_d<128>(a, nlse2, ndelta, dev, stream)
+                    : launch_bwd_d<64>(a, nlse2, ndelta, dev, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -236,10 +335,29 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                         int H, int Hkv, int64_t S, int D, int P, ra_layout layout, int causal,
                         float scale, void* stream) {
-  (void)q; (void)k; (void)v; (void)out; (void)lse; (void)dout; (void)dq; (void)dk; (void)dv;
-  (void)B; (void)H; (void)Hkv; (void)S; (void)D; (void)P; (void)layout; (void)causal;
-  (void)scale; (void)stream;
-  return fail(RA_ERR_UNSUPPORTED, "backward kernels are not built into this library yet");
+  BwdArgs a{q, k, v, out, lse, dout, dq, dk, dv, B, H, Hkv, S, D, P, (int)layout, causal, scale};
+  ra_status st = check_bwd(a);
+  if (st != RA_OK) return st;
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != RA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const ra::Geo g = ra::make_geo(B, H, Hkv, S, P, (int)layout, causal ? 1 : 0);
+  const size_t vec_bytes = (size_t)ra::vec_elems(g) * sizeof(float);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, 2 * vec_bytes, cs);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(RA_ERR_ALLOC, "cudaMallocAsync(%zu bytes) for the backward workspace: %s",
+                2 * vec_bytes, cudaGetErrorString(e));
+  }
+  float* nlse2 = static_cast<float*>(ws);
+  float* ndelta = reinterpret_cast<float*>(static_cast<char*>(ws) + vec_bytes);
+  st = bwd_launch(a, nlse2, ndelta, cs);
+  e = cudaFreeAsync(ws, cs);
+  if (st != RA_OK) return st;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(backward workspace)");
+  return RA_OK;
 }
 
 ra_status ring_attn_step(const void* q_shard, const void* k_shard, const void* v_shard,
