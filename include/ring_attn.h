@@ -134,6 +134,33 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
                         int causal, float scale, void* stream);
 
 /*
+ * ring_attn_bwd_noalloc -- ring_attn_bwd for callers that cannot allocate GPU
+ * memory while they run: a framework that has already reserved the whole
+ * device for its own caching allocator (so a driver allocation from inside
+ * a library fails or fragments that pool), or a program whose policy forbids
+ * allocation after start-up.  The pages have no counterpart of this call; it
+ * only changes where the backward's scratch lives.
+ *   Arguments, layouts, results and checks are those of ring_attn_bwd.  The
+ *   caller still passes every input and output.
+ *   The scratch (-lse*log2(e) and -delta in tile order) is a 16 MiB array that
+ *   the library reserves statically on every GPU that loads it, held until
+ *   the process exits.  Limit: B * H * P * T * 128 <= 2097152 (T = 128-slot
+ *   tiles per shard, counted per zig-zag chunk); larger problems get
+ *   RA_ERR_SHAPE with a message, and should use ring_attn_bwd.
+ *   No cudaMalloc, cudaMallocAsync, cudaFree or other allocating call is made.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call shares the one array and it keeps the last call's contents;
+ *   each call writes every scratch element it reads before reading it, so
+ *   nothing needs clearing.  Calls whose kernels overlap on the GPU (other
+ *   streams, other host threads) race on the array: serialise them.
+ */
+ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                int B, int H, int Hkv, int64_t S, int D, int P, ra_layout layout,
+                                int causal, float scale, void* stream);
+
+/*
  * ring_attn_step -- one ring hop: the queries of shard r against the key/value
  * block of shard s only ("Tiefer Einblick": as each block arrives the GPU
  * computes a partial attention), causal on global positions, normalised

@@ -48,6 +48,7 @@ def lib() -> ctypes.CDLL:
                                                 i32, i32, i32, f32, vp, vp]
             L.ring_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64,
                                         i32, i32, i32, i32, f32, vp]
+            L.ring_attn_bwd_noalloc.argtypes = L.ring_attn_bwd.argtypes
             L.ring_attn_step.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, i32, i32,
                                          i32, i32, i32, f32, vp]
             L.ring_attn_merge.argtypes = [vp, vp, vp, vp, i32, i32, i64, i32, vp]
@@ -58,6 +59,7 @@ def lib() -> ctypes.CDLL:
             L.ring_attn_last_error.restype = ctypes.c_char_p
             L.ring_attn_version.restype = ctypes.c_char_p
             for name in ("ring_attn_fwd", "ring_attn_fwd_counted", "ring_attn_bwd",
+                         "ring_attn_bwd_noalloc",
                          "ring_attn_step", "ring_attn_merge", "ring_attn_permute",
                          "ring_attn_index_map", "ring_attn_census", "ring_attn_check_status"):
                 getattr(L, name).restype = ctypes.c_int
@@ -144,6 +146,25 @@ def bwd(q, k, v, out, lse, dout, P: int, layout, causal: bool = True,
                                _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, P,
                                _layout(layout), int(bool(causal)), float(scale),
                                _stream(stream)))
+    return dq, dk, dv
+
+
+def bwd_noalloc(q, k, v, out, lse, dout, P: int, layout, causal: bool = True,
+                scale: float | None = None, dq=None, dk=None, dv=None, stream=None):
+    """bwd through ring_attn_bwd_noalloc: the library's scratch is its fixed
+    device array, so the call itself allocates nothing.  Pass dq, dk and dv to
+    keep this wrapper from allocating the outputs as well."""
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = D ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib().ring_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                       _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S,
+                                       D, P, _layout(layout), int(bool(causal)), float(scale),
+                                       _stream(stream)))
     return dq, dk, dv
 
 

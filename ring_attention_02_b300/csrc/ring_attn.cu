@@ -303,6 +303,35 @@ ra_status bwd_launch(const BwdArgs& a, float* nlse2, float* ndelta, cudaStream_t
                     : launch_bwd_d<64>(a, nlse2, ndelta, dev, stream);
 }
 
+// ---------------------------------------------------------------- fixed backward workspace
+// ring_attn_bwd_noalloc runs the backward on this statically sized device
+// array instead of a cudaMallocAsync workspace.  Every GPU that loads the
+// library holds it (16 MiB) until the process exits.  Host code must never
+// pass the array's name to a kernel: on the host it is only a stand-in
+// symbol.  The device address comes from cudaGetSymbolAddress, looked up
+// once per device with that device current.
+constexpr int64_t kFixedVecMax = int64_t(1) << 21;  // floats per vector (-lse*log2e, -delta)
+static __device__ __align__(256) float g_bwd_fixed_ws[2 * kFixedVecMax];
+
+std::mutex g_fixed_mu;
+float* g_fixed_ws_ptr[64] = {nullptr};
+
+ra_status fixed_workspace(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(RA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_fixed_mu);
+  if (g_fixed_ws_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_bwd_fixed_ws);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed backward workspace)");
+    g_fixed_ws_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_fixed_ws_ptr[dev];
+  return RA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -358,6 +387,30 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
   if (st != RA_OK) return st;
   if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(backward workspace)");
   return RA_OK;
+}
+
+ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                int B, int H, int Hkv, int64_t S, int D, int P, ra_layout layout,
+                                int causal, float scale, void* stream) {
+  BwdArgs a{q, k, v, out, lse, dout, dq, dk, dv, B, H, Hkv, S, D, P, (int)layout, causal, scale};
+  ra_status st = check_bwd(a);
+  if (st != RA_OK) return st;
+  const ra::Geo g = ra::make_geo(B, H, Hkv, S, P, (int)layout, causal ? 1 : 0);
+  const int64_t need = ra::vec_elems(g);
+  if (need > kFixedVecMax)
+    return fail(RA_ERR_SHAPE,
+                "ring_attn_bwd_noalloc: this problem needs a workspace of 2 x %lld floats "
+                "(B*H*P*T*128 with T 128-slot tiles per shard); the fixed workspace holds "
+                "2 x %lld.  Use ring_attn_bwd instead",
+                (long long)need, (long long)kFixedVecMax);
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != RA_OK) return st;
+  float* ws = nullptr;
+  st = fixed_workspace(&ws);
+  if (st != RA_OK) return st;
+  return bwd_launch(a, ws, ws + kFixedVecMax, static_cast<cudaStream_t>(stream));
 }
 
 ra_status ring_attn_step(const void* q_shard, const void* k_shard, const void* v_shard,
