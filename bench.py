@@ -5,8 +5,12 @@ every ring step, online-softmax accumulation, normalised output and lse).
 Default workload: B=1, H=32, Hkv=8, S=131072, D=128, P=16 virtual shards,
 zig-zag layout, causal, bf16 inputs drawn from N(0, 1).
 
+With a training workload (``--workload train-B2H16S32768D128P8``) one step
+is ``ring_attn_fwd`` followed by ``ring_attn_bwd`` (dq, dk, dv from a seeded
+dO), counted as 3.5x the forward's flops.
+
 Prints one JSON line.  ``--impl reference`` times the CPU oracle instead
-(bounded row samples of the same workload on the host cores).
+(bounded samples of the same workload on the host cores).
 """
 from __future__ import annotations
 
@@ -25,11 +29,12 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from ring_attention_02_b300.inputs import HEADLINE, Workload, by_name, make_for  # noqa: E402
+from ring_attention_02_b300.inputs import (HEADLINE, Workload, by_name, make_dout,  # noqa: E402
+                                           make_for)
 
 METRIC = "causal ring-attn fwd TFLOP/s (bf16, S=128k, 1 B300) and % of BF16 tensor peak"
+METRIC_TRAIN = "causal ring-attn fwd+bwd TFLOP/s (bf16, 1 B300; bwd counted as 2.5x fwd)"
 UNIT = "TFLOP/s"
-L2_NOTE = "inputs larger than L2 (1.5 GiB of q/k/v, 126 MB L2); no flush"
 
 
 def _dist():
@@ -56,8 +61,15 @@ def max_over_ranks(x: float) -> float:
 
 
 def config_of(w: Workload) -> dict:
+    qkv = w.B * w.S * (w.H + 2 * w.Hkv) * w.D * 2
+    l2 = (f"inputs larger than L2 ({qkv / 2**30:.2f} GiB of q/k/v, 126 MB L2); no flush"
+          if qkv > 126e6 else "inputs smaller than L2: repeated steps may hit in L2")
     return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "S": w.S, "D": w.D, "P": w.P,
-            "layout": w.layout, "causal": w.causal, "l2": L2_NOTE}
+            "layout": w.layout, "causal": w.causal, "backward": w.backward, "l2": l2}
+
+
+def metric_of(w: Workload) -> str:
+    return METRIC_TRAIN if w.backward else METRIC
 
 
 # ---------------------------------------------------------------- clocks
@@ -135,14 +147,38 @@ def measured_peaks():
     return 1800.0, 1400.0, "of fallback"
 
 
-def traffic_from_profiles():
-    """Per-launch DRAM bytes of the forward kernel from the committed ncu summary."""
-    path = os.path.join(ROOT, "profiles", "attn_fwd_headline_dram.json")
-    if os.path.exists(path):
-        with open(path) as f:
-            d = json.load(f)
-        return d.get("bytes_per_launch")
-    return None
+FWD_SOURCES = ["attn_fwd.cuh", "geometry.cuh", "sm103_ptx.cuh"]
+
+
+def fwd_source_digest() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in FWD_SOURCES:
+        with open(os.path.join(ROOT, "ring_attention_02_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_from_profiles(w: Workload):
+    """DRAM bytes per launch of the forward kernel on this workload, from the
+    committed ncu summary, or None when there is none or the kernel sources
+    changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_traffic_{w.name}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for ln in f:
+            if ":" in ln and not ln.startswith("#"):
+                key, val = ln.split(":", 1)
+                vals[key.strip()] = val.strip()
+    if vals.get("kernel_sources_sha256") != fwd_source_digest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 # ---------------------------------------------------------------- CPU oracle leg
@@ -158,6 +194,24 @@ def oracle_sample(w: Workload, q, k, v, rows_per_step: int, seed: int):
     oracle.attn_fwd_rows(qr, rows, k, v, w.causal, w.scale)
     dt = time.perf_counter() - t0
     return flops, dt
+
+
+def oracle_train_sample(w: Workload, q, k, v, do, prefix: int):
+    """Times the fp64 oracle's forward+backward on one (b, kv head) pair over
+    the first `prefix` tokens (a causal prefix is a whole problem of its own)."""
+    import oracle  # test infrastructure: the CPU-baseline leg only
+
+    G = w.H // w.Hkv
+    sl = slice(0, prefix)
+    f64 = lambda t: t[:1, sl].float().cpu().numpy().astype(np.float64)
+    qs = f64(q[:, :, :G])
+    ks, vs = f64(k[:, :, :1]), f64(v[:, :, :1])
+    dos = f64(do[:, :, :G])
+    flops = 3.5 * 4.0 * G * prefix * prefix * w.D / (2 if w.causal else 1)
+    t0 = time.perf_counter()
+    oracle.attn_fwd(qs, ks, vs, w.causal, w.scale)
+    oracle.attn_bwd(qs, ks, vs, dos, w.causal, w.scale, [(0, 0)])
+    return flops, time.perf_counter() - t0
 
 
 def host_kv(k, v):
@@ -177,18 +231,30 @@ def run_reference(args, w: Workload, rank: int):
         return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     q, k, v = make_for(w, seed=args.seed, device=dev)
-    kh, vh = host_kv(k, v)
-    rows = args.ref_rows
-    for i in range(args.warmup):
-        oracle_sample(w, q, kh, vh, rows, seed=1000 + i)
     tot_f, tot_t = 0.0, 0.0
-    for i in range(args.steps):
-        f, t = oracle_sample(w, q, kh, vh, rows, seed=i)
-        tot_f += f
-        tot_t += t
+    if w.backward:
+        do = make_dout(w.B, w.H, w.S, w.D, seed=args.seed, device=dev)
+        prefix = args.ref_prefix
+        for i in range(args.warmup):
+            oracle_train_sample(w, q, k, v, do, min(prefix, 512))
+        for i in range(args.steps):
+            f, t = oracle_train_sample(w, q, k, v, do, prefix)
+            tot_f += f
+            tot_t += t
+        sample = (f"fwd+bwd of (b=0, kv head 0) over the first {prefix} tokens per step, "
+                  f"fp64 C oracle")
+    else:
+        kh, vh = host_kv(k, v)
+        rows = args.ref_rows
+        for i in range(args.warmup):
+            oracle_sample(w, q, kh, vh, rows, seed=1000 + i)
+        for i in range(args.steps):
+            f, t = oracle_sample(w, q, kh, vh, rows, seed=i)
+            tot_f += f
+            tot_t += t
+        sample = f"{rows} query rows x {w.B * w.H} (b,h) per step, uniform positions, fp64 C oracle"
     val = tot_f / tot_t / 1e12
-    sample = f"{rows} query rows x {w.B * w.H} (b,h) per step, uniform positions, fp64 C oracle"
-    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1,
+    line = {"impl": "reference", "metric": metric_of(w), "value": val, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_of(w),
@@ -198,22 +264,19 @@ def run_reference(args, w: Workload, rank: int):
     print(json.dumps(line), flush=True)
 
 
-def measure_e2e(w, api, q, k, v, out, lse, stream, dev, flops, world, steps):
-    """Same metric through the public call with host buffers: each step copies
-    q/k/v from pinned host memory, runs ring_attn_fwd and copies out and lse
-    back, all inside the timed region."""
-    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
-    outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+def measure_e2e(w, api, step_fn, dev_in, dev_out, stream, dev, flops, world, steps):
+    """Same metric through the public calls with host buffers: each step copies
+    its inputs from pinned host memory, runs the step and copies its results
+    back to pinned host memory, all inside the timed region."""
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out]
 
     def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        api.fwd(qd, kd, vd, w.P, w.layout, w.causal, out=out, lse=lse, stream=stream)
-        outh.copy_(out, non_blocking=True)
-        lseh.copy_(lse, non_blocking=True)
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        step_fn()
+        for h, d in zip(host_out, dev_out):
+            h.copy_(d, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -227,8 +290,8 @@ def measure_e2e(w, api, q, k, v, out, lse, stream, dev, flops, world, steps):
     torch.cuda.synchronize(dev)
     api.check_status(stream)
     ms = max_over_ranks(e0.elapsed_time(e1)) / n
-    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
-    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in dev_in)
+    d2h = sum(t.numel() * t.element_size() for t in dev_out)
     return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
@@ -243,17 +306,30 @@ def run_ours(args, w: Workload, rank: int, world: int):
     q, k, v = make_for(w, seed=args.seed + 17 * rank, device=dev)
     out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    if w.backward:
+        do = make_dout(w.B, w.H, w.S, w.D, seed=args.seed + 17 * rank, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
-    def step():
+    # events: [fwd start, fwd end (= bwd start), bwd end] per timed step
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+
+    def step(i=None):
+        if i is not None:
+            marks[i][0].record(stream)
         api.fwd(q, k, v, w.P, w.layout, w.causal, out=out, lse=lse, stream=stream)
+        if i is not None:
+            marks[i][1].record(stream)
+        if w.backward:
+            api.bwd(q, k, v, out, lse, do, w.P, w.layout, w.causal, dq=dq, dk=dk, dv=dv,
+                    stream=stream)
+            if i is not None:
+                marks[i][2].record(stream)
 
     for _ in range(args.warmup):
         step()
     api.check_status(stream)
 
     # ---- device-resident timed region
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     _barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
@@ -261,29 +337,43 @@ def run_ours(args, w: Workload, rank: int, world: int):
         t_all1 = torch.cuda.Event(enable_timing=True)
         t_all0.record(stream)
         for i in range(args.steps):
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
+            step(i)
         t_all1.record(stream)
         torch.cuda.synchronize(dev)
     _barrier()
     api.check_status(stream)
-    total_ms = t_all0.elapsed_time(t_all1)
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = max_over_ranks(total_ms)
+    total_ms = max_over_ranks(t_all0.elapsed_time(t_all1))
     ms_per_step = total_ms / args.steps
-    flops = w.counted_flops()
+    flops = w.step_flops()
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    fwd_ms = [m[0].elapsed_time(m[1]) for m in marks]
+    bwd_ms = [m[1].elapsed_time(m[2]) for m in marks] if w.backward else []
 
-    # ---- end to end through host buffers (pinned), one C-ABI call per step
+    # ---- end to end through host buffers (pinned), C-ABI calls per step
     e2e = None
     if not args.skip_e2e:
-        e2e = measure_e2e(w, api, q, k, v, out, lse, stream, dev, flops, world, args.steps)
+        if w.backward:
+            e2e = measure_e2e(w, api, step, [q, k, v, do], [dq, dk, dv], stream, dev, flops,
+                              world, args.steps)
+        else:
+            e2e = measure_e2e(w, api, step, [q, k, v], [out, lse], stream, dev, flops, world,
+                              args.steps)
     if rank != 0:
         return
     peak, peak_sus, peak_src = measured_peaks()
-    avg_launch = sum(launch_ms) / len(launch_ms)
-    achieved = flops / (avg_launch * 1e-3) / 1e12
+    if w.backward:
+        # dominant call: the backward (prep + dK/dV pass + dQ pass)
+        dom_ms = sum(bwd_ms) / len(bwd_ms)
+        achieved = 2.5 * w.counted_flops() / (dom_ms * 1e-3) / 1e12
+        kernel = "ring_attn_bwd: bwd_prep_kernel + attn_bwd_dkdv_kernel + attn_bwd_dq_kernel"
+        traffic = None
+        launches = 4 * args.steps
+    else:
+        dom_ms = sum(fwd_ms) / len(fwd_ms)
+        achieved = w.counted_flops() / (dom_ms * 1e-3) / 1e12
+        kernel = f"attn_fwd_kernel<{w.D}>"
+        traffic = traffic_from_profiles(w)
+        launches = args.steps
     pairs, tiles = api.census(w.S, w.P, w.layout, w.causal)
     tiles = tiles.double()
     imbalance = float(tiles.max() / tiles.mean() - 1.0)
@@ -291,32 +381,41 @@ def run_ours(args, w: Workload, rank: int, world: int):
     # CPU oracle on a bounded sample (rank 0, N=1 only)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        kh, vh = host_kv(k, v)
         f_s, t_s = 0.0, 0.0
-        while t_s < args.cpu_seconds:
-            f, t = oracle_sample(w, q, kh, vh, 64, seed=int(t_s * 1000) + 7)
-            f_s += f
-            t_s += t
+        if w.backward:
+            f_s, t_s = oracle_train_sample(w, q, k, v, do, args.ref_prefix)
+            sample = (f"fwd+bwd of (b=0, kv head 0) over the first {args.ref_prefix} tokens, "
+                      f"{t_s:.1f} s of fp64 C oracle, {f_s:.3g} counted flop")
+        else:
+            kh, vh = host_kv(k, v)
+            while t_s < args.cpu_seconds:
+                f, t = oracle_sample(w, q, kh, vh, 64, seed=int(t_s * 1000) + 7)
+                f_s += f
+                t_s += t
+            sample = (f"uniform query rows x {w.B * w.H} (b,h), {t_s:.1f} s of fp64 C oracle, "
+                      f"{f_s:.3g} counted flop")
         cpu = {"value": f_s / t_s / 1e12, "unit": UNIT, "cores": cores(), "kind": "oracle",
-               "sample": f"uniform query rows x {w.B * w.H} (b,h), {t_s:.1f} s of fp64 C oracle, "
-                         f"{f_s:.3g} counted flop"}
+               "sample": sample}
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w),
+        "metric": metric_of(w), "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_of(w),
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": traffic_from_profiles(),
+                     "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"bf16 burst {peak_src}", "peak_sustained": peak_sus,
-                     "kernel": "attn_fwd_kernel<128>"},
+                     "kernel": kernel},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": launches,
         "clocks": clk.summary(),
         "shard_imbalance": imbalance,
     }
+    if w.backward:
+        line["fwd_ms"] = sum(fwd_ms) / len(fwd_ms)
+        line["bwd_ms"] = sum(bwd_ms) / len(bwd_ms)
     print(json.dumps(line), flush=True)
 
 
@@ -333,6 +432,8 @@ def main(argv=None):
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--ref-prefix", type=int, default=12288,
+                    help="training workloads: tokens of the oracle's fwd+bwd sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -133,15 +133,16 @@ def fwd_counted(q, k, v, P: int, layout, causal: bool = True, scale: float | Non
 
 
 def bwd(q, k, v, out, lse, dout, P: int, layout, causal: bool = True,
-        scale: float | None = None, stream=None):
-    """Gradients (dq, dk, dv), bf16, natural order."""
+        scale: float | None = None, dq=None, dk=None, dv=None, stream=None):
+    """Gradients (dq, dk, dv), bf16, natural order (written into dq, dk, dv
+    when given)."""
     B, S, H, D = q.shape
     Hkv = k.shape[2]
     if scale is None:
         scale = D ** -0.5
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(k)
-    dv = torch.empty_like(v)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
     _check(lib().ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
                                _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, P,
                                _layout(layout), int(bool(causal)), float(scale),

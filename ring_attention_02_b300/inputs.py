@@ -47,6 +47,11 @@ class Workload:
         f = 4.0 * self.B * self.H * self.S * self.S * self.D
         return f / 2 if self.causal else f
 
+    def step_flops(self) -> float:
+        """Counted flops of one step: the forward, plus 2.5x the forward for
+        the backward (five matrix products against the forward's two)."""
+        return self.counted_flops() * (3.5 if self.backward else 1.0)
+
 
 # The five problems the library is measured and checked on.
 TINY = Workload("tiny-noncausal-B1H2S256D64P4", 1, 2, 2, 256, 64, 4, "contiguous", False,
@@ -62,12 +67,15 @@ WORKLOADS = [TINY, CAUSAL_8K, GQA_128K, MILLION, TRAIN_32K]
 # A mid-size causal forward for profiler captures: 192 MiB of q/k/v (larger
 # than the 126 MB L2) and a few milliseconds per launch.
 PROFILE_32K = Workload("causal-B1H8S32768D128P8", 1, 8, 8, 32768, 128, 8, "zigzag", True)
+# A smaller training step for profiler captures of the backward kernels.
+PROFILE_TRAIN_16K = Workload("train-B1H16S16384D128P8", 1, 16, 16, 16384, 128, 8, "zigzag",
+                             True, backward=True)
 # The headline forward: the 128k GQA shapes with the zig-zag layout.
 HEADLINE = GQA_128K.with_layout("zigzag")
 
 
 def by_name(name: str) -> Workload:
-    for w in WORKLOADS + [HEADLINE, PROFILE_32K]:
+    for w in WORKLOADS + [HEADLINE, PROFILE_32K, PROFILE_TRAIN_16K]:
         if w.name == name:
             return w
     raise KeyError(name)
