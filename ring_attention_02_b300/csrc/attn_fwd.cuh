@@ -13,14 +13,18 @@
 // Roles (384 threads):
 //   warp 0       TMA producer: Q tiles once per unit, K and V tiles through a
 //                ring of shared-memory stages (mbarrier full/empty pairs);
-//   warp 1       MMA issuer: S_x = Q_x K^T (both operands in shared memory)
-//                and O_x += P_x V (P read from tensor memory), tcgen05.mma
-//                issued by one thread, completion signalled by tcgen05.commit;
-//                the whole warp owns the TMEM allocation;
+//   warps 1, 3   MMA issuers, one thread each: warp 1 for query tile A,
+//                warp 3 for tile B.  Each issues S_x = Q_x K^T (both operands
+//                in shared memory) and O_x += P_x V (P read from tensor
+//                memory) with tcgen05.mma and signals completion with
+//                tcgen05.commit; warp 1 owns the TMEM allocation;
 //   warps 4..7   softmax of query tile A, one row per thread;
 //   warps 8..11  softmax of query tile B.
-// The two softmax warpgroups ping-pong: while one turns S into P the tensor
-// core runs the other tile's P V and next Q K^T.
+// The two tiles run independent chains (S -> softmax -> P V -> next S) and
+// the tensor core interleaves them: while one tile's softmax turns S into P,
+// the other tile's products run.  A single issuing thread would serialise the
+// two chains behind its own barrier waits and commits; measured on a B300 the
+// second issuer raises the 32k causal forward from 1041 to 1111 TFLOP/s.
 //
 // Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D),
 // O_B [384,384+D).  P (bf16, two per column) overwrites the first 64 columns
@@ -83,7 +87,7 @@ struct __align__(1024) FwdSmem {
   uint64_t k_full[FwdCfg<D>::kKStages], k_empty[FwdCfg<D>::kKStages];
   uint64_t v_full[FwdCfg<D>::kVStages], v_empty[FwdCfg<D>::kVStages];
   uint64_t s_full[2], p_full[2], o_full[2];
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -197,13 +201,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     for (int i = 0; i < Cfg::kKStages; ++i) {
       mbar_init(smem_u32(&sm.k_full[i]), 1);
-      mbar_init(smem_u32(&sm.k_empty[i]), 1);
+      mbar_init(smem_u32(&sm.k_empty[i]), 2);
     }
     for (int i = 0; i < Cfg::kVStages; ++i) {
       mbar_init(smem_u32(&sm.v_full[i]), 1);
-      mbar_init(smem_u32(&sm.v_empty[i]), 1);
+      mbar_init(smem_u32(&sm.v_empty[i]), 2);
     }
-    mbar_init(smem_u32(&sm.drain), 1);
+    mbar_init(smem_u32(&sm.drain[0]), 1);
+    mbar_init(smem_u32(&sm.drain[1]), 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -286,11 +291,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           ++it.bt;
         }
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if ((warp == 1 || warp == 3) && lane == 0) {
+      // ---------------------------------------------------------- MMA issuers
+      // One thread per query tile (warp 1: tile A, warp 3: tile B), each with
+      // its own chain S_x = Q_x K^T -> softmax_x -> O_x += P_x V.  The tensor
+      // core interleaves the two streams.  A key / value stage is released
+      // when both issuers have committed it (barrier count 2), and each issuer
+      // waits for every stage it passes, so neither can run a full ring ahead.
+      const int x = warp == 1 ? 0 : 1;
       constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16(128, D, false, true);
-      uint32_t q_ph0 = 0, q_ph1 = 0, p_ph0 = 0, p_ph1 = 0;
+      uint32_t q_ph = 0, p_ph = 0;
       uint32_t kst = 0, k_ph = 0, vst = 0, v_ph = 0;
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
@@ -300,73 +311,65 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const QTile qb = make_qtile(g, u.shard, u.seg, 2 * u.pair + 1);
         const int na = tile_work(g, qa, sblk), nb = tile_work(g, qb, sblk);
         if (na + nb == 0) continue;
-        if (p.shard_tiles != nullptr)
+        if (x == 0 && p.shard_tiles != nullptr)
           atomicAdd(p.shard_tiles + u.shard, static_cast<unsigned long long>(na + nb));
-        int cnt_s0 = 0, cnt_s1 = 0, cnt_pv0 = 0, cnt_pv1 = 0;
-        bool pend0 = false, pend1 = false;   // a P V of the previous key tile is owed
+        const QTile& qt = x ? qb : qa;
+        const int nx = x ? nb : na;
+        int cnt_s = 0, cnt_pv = 0;
+        bool pend = false;   // a P V of the previous key tile is owed
         int prev_vst = -1;
         KIter it;
         kiter_setup(p, u.shard, qb.valid && qb.qmax > qa.qmax ? qb.qmax : qa.qmax, it);
         bool more = kiter_next(p, it);
         while (true) {
-          bool act0 = false, act1 = false;
+          bool act = false;
           if (more) {
-            act0 = visible_to(p, it, qa.valid, qa.qmax);
-            act1 = visible_to(p, it, qb.valid, qb.qmax);
+            act = visible_to(p, it, qt.valid, qt.qmax);
             if (!mbar_wait(smem_u32(&sm.k_full[kst]), k_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
               goto done;
             tc_fence_after();
           }
-          if (pend0 || pend1) {
+          if (prev_vst >= 0) {
             if (!mbar_wait(smem_u32(&sm.v_full[prev_vst]), v_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
               goto done;
             tc_fence_after();
           }
+          if (pend) {
+            // O_x += P_x V_prev
+            if (!mbar_wait(smem_u32(&sm.p_full[x]), p_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
+              goto done;
+            p_ph ^= 1;
+            tc_fence_after();
+            const uint32_t vb = smem_u32(sm.v[prev_vst]);
 #pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            bool& pend = x ? pend1 : pend0;
-            int& cnt_pv = x ? cnt_pv1 : cnt_pv0;
-            int& cnt_s = x ? cnt_s1 : cnt_s0;
-            uint32_t& p_ph = x ? p_ph1 : p_ph0;
-            uint32_t& q_ph = x ? q_ph1 : q_ph0;
-            const int nx = x ? nb : na;
-            if (pend) {
-              // O_x += P_x V_prev
-              if (!mbar_wait(smem_u32(&sm.p_full[x]), p_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8,
+                     sdesc_sw128(vb + kk * 2048, kTile * 128, 1024), id_pv,
+                     (cnt_pv > 0 || kk > 0) ? 1u : 0u);
+            ++cnt_pv;
+            pend = false;
+            if (cnt_pv == nx) mma_commit(smem_u32(&sm.o_full[x]));
+          }
+          if (more && act) {
+            if (cnt_s == 0) {
+              if (!mbar_wait(smem_u32(&sm.q_full[x]), q_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
                 goto done;
-              p_ph ^= 1;
+              q_ph ^= 1;
               tc_fence_after();
-              const uint32_t vb = smem_u32(sm.v[prev_vst]);
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                mma_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8,
-                       sdesc_sw128(vb + kk * 2048, kTile * 128, 1024), id_pv,
-                       (cnt_pv > 0 || kk > 0) ? 1u : 0u);
-              ++cnt_pv;
-              pend = false;
-              if (cnt_pv == nx) mma_commit(smem_u32(&sm.o_full[x]));
             }
-            if (more && (x ? act1 : act0)) {
-              if (cnt_s == 0) {
-                if (!mbar_wait(smem_u32(&sm.q_full[x]), q_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
-                  goto done;
-                q_ph ^= 1;
-                tc_fence_after();
-              }
-              // S_x = Q_x K^T
-              const uint32_t qbase = smem_u32(sm.q[x]);
-              const uint32_t kbase = smem_u32(sm.k[kst]);
+            // S_x = Q_x K^T
+            const uint32_t qbase = smem_u32(sm.q[x]);
+            const uint32_t kbase = smem_u32(sm.k[kst]);
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
-                mma_ss(tmem + col_s(x), sdesc_sw128(qbase + off, 16, 1024),
-                       sdesc_sw128(kbase + off, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(smem_u32(&sm.s_full[x]));
-              ++cnt_s;
-              if (cnt_s == nx) mma_commit(smem_u32(&sm.q_empty[x]));
-              pend = true;
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
+              mma_ss(tmem + col_s(x), sdesc_sw128(qbase + off, 16, 1024),
+                     sdesc_sw128(kbase + off, 16, 1024), id_qk, kk > 0 ? 1u : 0u);
             }
+            mma_commit(smem_u32(&sm.s_full[x]));
+            ++cnt_s;
+            if (cnt_s == nx) mma_commit(smem_u32(&sm.q_empty[x]));
+            pend = true;
           }
           if (prev_vst >= 0) {
             mma_commit(smem_u32(&sm.v_empty[prev_vst]));
@@ -613,9 +616,10 @@ done:
   __syncthreads();
   if (sm.abort_flag) {
     // Let whatever was issued before the failure land before TMEM goes away.
-    if (warp == 1 && lane == 0) {
-      mma_commit(smem_u32(&sm.drain));
-      mbar_wait(smem_u32(&sm.drain), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
+    if ((warp == 1 || warp == 3) && lane == 0) {
+      const int x = warp == 1 ? 0 : 1;
+      mma_commit(smem_u32(&sm.drain[x]));
+      mbar_wait(smem_u32(&sm.drain[x]), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
     }
     const unsigned long long t0 = globaltimer();
     while (globaltimer() - t0 < 1000000ull) {
