@@ -29,7 +29,8 @@
 //
 // Roles in both tensor-core kernels (384 threads, one persistent CTA per SM):
 //   warp 0       TMA producer,
-//   warp 1       tcgen05 issuer (one thread) and owner of the TMEM allocation,
+//   warps 1, 3   tcgen05 issuers, one thread each (see each kernel); warp 1
+//                owns the TMEM allocation,
 //   warps 4..7   "half 0": columns [0, 64) of every S / dP tile,
 //   warps 8..11  "half 1": columns [64, 128).
 // The S / dP products are issued per half (N = 64), so half 0's elementwise
@@ -294,7 +295,7 @@ struct __align__(1024) DkdvSmem {
   uint64_t st_full[BwdCfg<D>::kStages], st_empty[BwdCfg<D>::kStages];
   uint64_t s_full[2], p_full[2];
   uint64_t acc_full, acc_empty;
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -309,7 +310,7 @@ struct __align__(1024) DqSmem {
   uint64_t st_full[BwdCfg<D>::kStages], st_empty[BwdCfg<D>::kStages];
   uint64_t s_full[2], p_full[2];
   uint64_t acc_full, acc_empty;
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -372,18 +373,19 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
   if (tid == 0) {
     mbar_init(smem_u32(&sm.kv_full), 1);
-    mbar_init(smem_u32(&sm.kv_empty), 1);
+    mbar_init(smem_u32(&sm.kv_empty), 2);
     for (int i = 0; i < kSt; ++i) {
       mbar_init(smem_u32(&sm.st_full[i]), 1);
-      mbar_init(smem_u32(&sm.st_empty[i]), 1);
+      mbar_init(smem_u32(&sm.st_empty[i]), 2);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(smem_u32(&sm.s_full[x]), 1);
+      mbar_init(smem_u32(&sm.s_full[x]), 2);
       mbar_init(smem_u32(&sm.p_full[x]), 128);
     }
-    mbar_init(smem_u32(&sm.acc_full), 1);
+    mbar_init(smem_u32(&sm.acc_full), 2);
     mbar_init(smem_u32(&sm.acc_empty), 256);
-    mbar_init(smem_u32(&sm.drain), 1);
+    mbar_init(smem_u32(&sm.drain[0]), 1);
+    mbar_init(smem_u32(&sm.drain[1]), 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -455,28 +457,36 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         } while (qiter_next(g, it));
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 3) {
     if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
+      // ------------------------------------------------------------ MMA issuers
+      // Issuer 0 (warp 1): S^T_x = K Q_x^T and dV += P^T_x dO_x.
+      // Issuer 1 (warp 3): dP^T_x = V dO_x^T and dK += dS^T_x Q_x.
+      // Each accumulator has one issuer; s_full, st_empty, kv_empty and
+      // acc_full complete when both have committed.
+      const int w = warp == 1 ? 0 : 1;
       uint32_t kv_ph = 0, st = 0, st_ph = 0, p_ph0 = 0, p_ph1 = 0, acc_ph = 0;
-      const uint32_t kb = smem_u32(sm.k), vb = smem_u32(sm.v);
+      const uint32_t a_op = w == 0 ? smem_u32(sm.k) : smem_u32(sm.v);
+      const uint32_t prod_col = w == 0 ? kColS : kColDP;    // product written, then its bf16 half read
+      const uint32_t acc_col = w == 0 ? kColAcc0 : kColAcc1;
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
-        const KUnit w = kunit_of(g, item);
-        const QTile kt = make_qtile(g, w.shard, w.seg, w.tile);
+        const KUnit u = kunit_of(g, item);
+        const QTile kt = make_qtile(g, u.shard, u.seg, u.tile);
         QIter it;
-        qiter_setup(g, it, w.hkv, w.shard, kt.qmin);
+        qiter_setup(g, it, u.hkv, u.shard, kt.qmin);
         if (!kt.valid || !qiter_next(g, it)) continue;
         if (!mbar_wait(smem_u32(&sm.kv_full), kv_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
         kv_ph ^= 1;
         if (!mbar_wait(smem_u32(&sm.st_full[st]), st_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
         tc_fence_after();
-        // S^T_x = K Q_x^T and dP^T_x = V dO_x^T for both halves of the first tile
+        // B operand of the product: Q (issuer 0) or dO (issuer 1); of the accumulation: the other
+        auto prod_b = [&](uint32_t s_) { return w == 0 ? smem_u32(sm.q[s_]) : smem_u32(sm.dO[s_]); };
+        auto acc_b = [&](uint32_t s_) { return w == 0 ? smem_u32(sm.dO[s_]) : smem_u32(sm.q[s_]); };
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          issue_half_product<D>(tmem + kColS + 64 * x, kb, smem_u32(sm.q[st]), x);
-          issue_half_product<D>(tmem + kColDP + 64 * x, vb, smem_u32(sm.dO[st]), x);
+          issue_half_product<D>(tmem + prod_col + 64 * x, a_op, prod_b(st), x);
           mma_commit(smem_u32(&sm.s_full[x]));
         }
         bool first = true;
@@ -486,7 +496,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           const bool more = qiter_next(g, it);
           uint32_t nst = st + 1, nph = st_ph;
           if (nst == (uint32_t)kSt) { nst = 0; nph ^= 1; }
-          // half 0: dV += P^T_0 dO_0, dK += dS^T_0 Q_0
+          // half 0
           if (!mbar_wait(smem_u32(&sm.p_full[0]), p_ph0, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
           p_ph0 ^= 1;
           tc_fence_after();
@@ -495,31 +505,25 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
               goto done;
             tc_fence_after();
           }
-          issue_half_accumulate<D>(tmem + kColAcc0, tmem + kColS, smem_u32(sm.dO[cur]), 0, first);
-          issue_half_accumulate<D>(tmem + kColAcc1, tmem + kColDP, smem_u32(sm.q[cur]), 0, first);
+          issue_half_accumulate<D>(tmem + acc_col, tmem + prod_col, acc_b(cur), 0, first);
           if (more) {
             if (!mbar_wait(smem_u32(&sm.st_full[nst]), nph, RA_DEV_TIMEOUT_MMA, abort_flag))
               goto done;
             tc_fence_after();
-            issue_half_product<D>(tmem + kColS, kb, smem_u32(sm.q[nst]), 0);
-            issue_half_product<D>(tmem + kColDP, vb, smem_u32(sm.dO[nst]), 0);
+            issue_half_product<D>(tmem + prod_col, a_op, prod_b(nst), 0);
             mma_commit(smem_u32(&sm.s_full[0]));
           }
           // half 1
           if (!mbar_wait(smem_u32(&sm.p_full[1]), p_ph1, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
           p_ph1 ^= 1;
           tc_fence_after();
-          issue_half_accumulate<D>(tmem + kColAcc0, tmem + kColS + 64, smem_u32(sm.dO[cur]), 1,
-                                   false);
-          issue_half_accumulate<D>(tmem + kColAcc1, tmem + kColDP + 64, smem_u32(sm.q[cur]), 1,
-                                   false);
+          issue_half_accumulate<D>(tmem + acc_col, tmem + prod_col + 64, acc_b(cur), 1, false);
           mma_commit(smem_u32(&sm.st_empty[cur]));
           st = nst;
           st_ph = nph;
           first = false;
           if (!more) break;
-          issue_half_product<D>(tmem + kColS + 64, kb, smem_u32(sm.q[st]), 1);
-          issue_half_product<D>(tmem + kColDP + 64, vb, smem_u32(sm.dO[st]), 1);
+          issue_half_product<D>(tmem + prod_col + 64, a_op, prod_b(st), 1);
           mma_commit(smem_u32(&sm.s_full[1]));
         }
         mma_commit(smem_u32(&sm.acc_full));
@@ -629,9 +633,10 @@ done:
   tc_fence_before();
   __syncthreads();
   if (sm.abort_flag) {
-    if (warp == 1 && lane == 0) {
-      mma_commit(smem_u32(&sm.drain));
-      mbar_wait(smem_u32(&sm.drain), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
+    if ((warp == 1 || warp == 3) && lane == 0) {
+      const int w = warp == 1 ? 0 : 1;
+      mma_commit(smem_u32(&sm.drain[w]));
+      mbar_wait(smem_u32(&sm.drain[w]), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
     }
     const unsigned long long t0 = globaltimer();
     while (globaltimer() - t0 < 1000000ull) {
@@ -660,18 +665,19 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
   if (tid == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
-    mbar_init(smem_u32(&sm.q_empty), 1);
+    mbar_init(smem_u32(&sm.q_empty), 2);
     for (int i = 0; i < kSt; ++i) {
       mbar_init(smem_u32(&sm.st_full[i]), 1);
-      mbar_init(smem_u32(&sm.st_empty[i]), 1);
+      mbar_init(smem_u32(&sm.st_empty[i]), 2);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(smem_u32(&sm.s_full[x]), 1);
+      mbar_init(smem_u32(&sm.s_full[x]), 2);
       mbar_init(smem_u32(&sm.p_full[x]), 128);
     }
     mbar_init(smem_u32(&sm.acc_full), 1);
     mbar_init(smem_u32(&sm.acc_empty), 256);
-    mbar_init(smem_u32(&sm.drain), 1);
+    mbar_init(smem_u32(&sm.drain[0]), 1);
+    mbar_init(smem_u32(&sm.drain[1]), 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -742,19 +748,25 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         } while (kiterb_next(g, it));
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 3) {
     if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
+      // ------------------------------------------------------------ MMA issuers
+      // Issuer 0 (warp 1): S_x = Q K_x^T and dQ += dS_x K_x.
+      // Issuer 1 (warp 3): dP_x = dO V_x^T.
+      // s_full, st_empty and q_empty complete when both have committed.
+      const int w = warp == 1 ? 0 : 1;
       uint32_t q_ph = 0, st = 0, st_ph = 0, p_ph0 = 0, p_ph1 = 0, acc_ph = 0;
-      const uint32_t qb = smem_u32(sm.q), dob = smem_u32(sm.dO);
+      const uint32_t a_op = w == 0 ? smem_u32(sm.q) : smem_u32(sm.dO);
+      const uint32_t prod_col = w == 0 ? kColS : kColDP;
+      auto prod_b = [&](uint32_t s_) { return w == 0 ? smem_u32(sm.k[s_]) : smem_u32(sm.v[s_]); };
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
-        const QUnit w = qunit_of(g, item);
-        const QTile qt = make_qtile(g, w.shard, w.seg, w.tile);
+        const QUnit u = qunit_of(g, item);
+        const QTile qt = make_qtile(g, u.shard, u.seg, u.tile);
         if (!qt.valid) continue;
         KIterB it;
-        kiterb_setup(g, it, w.shard, qt.qmax);
+        kiterb_setup(g, it, u.shard, qt.qmax);
         if (!kiterb_next(g, it)) continue;
         if (!mbar_wait(smem_u32(&sm.q_full), q_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
         q_ph ^= 1;
@@ -762,8 +774,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tc_fence_after();
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          issue_half_product<D>(tmem + kColS + 64 * x, qb, smem_u32(sm.k[st]), x);
-          issue_half_product<D>(tmem + kColDP + 64 * x, dob, smem_u32(sm.v[st]), x);
+          issue_half_product<D>(tmem + prod_col + 64 * x, a_op, prod_b(st), x);
           mma_commit(smem_u32(&sm.s_full[x]));
         }
         bool first = true;
@@ -773,40 +784,41 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           const bool more = kiterb_next(g, it);
           uint32_t nst = st + 1, nph = st_ph;
           if (nst == (uint32_t)kSt) { nst = 0; nph ^= 1; }
-          // dQ += dS_0 K[0:64]
+          // half 0: dS_0 is in TMEM, dP_0 has been read
           if (!mbar_wait(smem_u32(&sm.p_full[0]), p_ph0, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
           p_ph0 ^= 1;
           tc_fence_after();
-          if (first) {
-            if (!mbar_wait(smem_u32(&sm.acc_empty), acc_ph ^ 1, RA_DEV_TIMEOUT_MMA, abort_flag))
-              goto done;
-            tc_fence_after();
+          if (w == 0) {
+            if (first) {
+              if (!mbar_wait(smem_u32(&sm.acc_empty), acc_ph ^ 1, RA_DEV_TIMEOUT_MMA, abort_flag))
+                goto done;
+              tc_fence_after();
+            }
+            issue_half_accumulate<D>(tmem + kColAcc0, tmem + kColS, smem_u32(sm.k[cur]), 0, first);
           }
-          issue_half_accumulate<D>(tmem + kColAcc0, tmem + kColS, smem_u32(sm.k[cur]), 0, first);
           if (more) {
             if (!mbar_wait(smem_u32(&sm.st_full[nst]), nph, RA_DEV_TIMEOUT_MMA, abort_flag))
               goto done;
             tc_fence_after();
-            issue_half_product<D>(tmem + kColS, qb, smem_u32(sm.k[nst]), 0);
-            issue_half_product<D>(tmem + kColDP, dob, smem_u32(sm.v[nst]), 0);
+            issue_half_product<D>(tmem + prod_col, a_op, prod_b(nst), 0);
             mma_commit(smem_u32(&sm.s_full[0]));
           }
-          // dQ += dS_1 K[64:128]
+          // half 1
           if (!mbar_wait(smem_u32(&sm.p_full[1]), p_ph1, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
           p_ph1 ^= 1;
           tc_fence_after();
-          issue_half_accumulate<D>(tmem + kColAcc0, tmem + kColS + 64, smem_u32(sm.k[cur]), 1,
-                                   false);
+          if (w == 0)
+            issue_half_accumulate<D>(tmem + kColAcc0, tmem + kColS + 64, smem_u32(sm.k[cur]), 1,
+                                     false);
           mma_commit(smem_u32(&sm.st_empty[cur]));
           st = nst;
           st_ph = nph;
           first = false;
           if (!more) break;
-          issue_half_product<D>(tmem + kColS + 64, qb, smem_u32(sm.k[st]), 1);
-          issue_half_product<D>(tmem + kColDP + 64, dob, smem_u32(sm.v[st]), 1);
+          issue_half_product<D>(tmem + prod_col + 64, a_op, prod_b(st), 1);
           mma_commit(smem_u32(&sm.s_full[1]));
         }
-        mma_commit(smem_u32(&sm.acc_full));
+        if (w == 0) mma_commit(smem_u32(&sm.acc_full));
         mma_commit(smem_u32(&sm.q_empty));
         acc_ph ^= 1;
       }
@@ -902,9 +914,10 @@ done:
   tc_fence_before();
   __syncthreads();
   if (sm.abort_flag) {
-    if (warp == 1 && lane == 0) {
-      mma_commit(smem_u32(&sm.drain));
-      mbar_wait(smem_u32(&sm.drain), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
+    if ((warp == 1 || warp == 3) && lane == 0) {
+      const int w = warp == 1 ? 0 : 1;
+      mma_commit(smem_u32(&sm.drain[w]));
+      mbar_wait(smem_u32(&sm.drain[w]), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
     }
     const unsigned long long t0 = globaltimer();
     while (globaltimer() - t0 < 1000000ull) {
