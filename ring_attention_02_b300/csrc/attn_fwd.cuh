@@ -20,11 +20,13 @@
 //                tcgen05.commit; warp 1 owns the TMEM allocation;
 //   warps 4..7   softmax of query tile A, one row per thread;
 //   warps 8..11  softmax of query tile B.
-// The two tiles run independent chains (S -> softmax -> P V -> next S) and
-// the tensor core interleaves them: while one tile's softmax turns S into P,
-// the other tile's products run.  A single issuing thread would serialise the
-// two chains behind its own barrier waits and commits; measured on a B300 the
-// second issuer raises the 32k causal forward from 1041 to 1111 TFLOP/s.
+// The two tiles run independent chains (S -> softmax -> P V -> next S).  The
+// issuers pass a turn back and forth (two mbarriers), so their batches
+// alternate on the tensor core: while one tile's softmax turns S into P, the
+// other tile's products run.  Measured on a B300 (32k causal forward): one
+// issuing thread 1041 TFLOP/s (its own barrier waits serialise both chains),
+// two free-running issuers 1111 (the chains fall into step, so both softmaxes
+// leave the tensor core idle together), two alternating issuers 1148.
 //
 // Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D),
 // O_B [384,384+D).  P (bf16, two per column) overwrites the first 64 columns
@@ -87,6 +89,7 @@ struct __align__(1024) FwdSmem {
   uint64_t k_full[FwdCfg<D>::kKStages], k_empty[FwdCfg<D>::kKStages];
   uint64_t v_full[FwdCfg<D>::kVStages], v_empty[FwdCfg<D>::kVStages];
   uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t turn[2];      // issuer x may issue its next batch
   uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -209,6 +212,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     mbar_init(smem_u32(&sm.drain[0]), 1);
     mbar_init(smem_u32(&sm.drain[1]), 1);
+    mbar_init(smem_u32(&sm.turn[0]), 1);
+    mbar_init(smem_u32(&sm.turn[1]), 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -301,7 +306,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int x = warp == 1 ? 0 : 1;
       constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16(128, D, false, true);
-      uint32_t q_ph = 0, p_ph = 0;
+      uint32_t q_ph = 0, p_ph = 0, turn_ph = 0;
+      bool first_turn = x == 0;   // tile A's issuer opens the alternation
       uint32_t kst = 0, k_ph = 0, vst = 0, v_ph = 0;
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
@@ -333,6 +339,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!mbar_wait(smem_u32(&sm.v_full[prev_vst]), v_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
               goto done;
             tc_fence_after();
+          }
+          // Batches alternate between the two issuers (A, B, A, B, ...), so
+          // one tile's softmax runs while the tensor core works on the other
+          // tile's batch; left free, the two chains fall into step and both
+          // softmaxes then leave the tensor core idle at the same time.
+          if (first_turn) {
+            first_turn = false;
+          } else {
+            if (!mbar_wait(smem_u32(&sm.turn[x]), turn_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
+              goto done;
+            turn_ph ^= 1;
           }
           if (pend) {
             // O_x += P_x V_prev
@@ -371,6 +388,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (cnt_s == nx) mma_commit(smem_u32(&sm.q_empty[x]));
             pend = true;
           }
+          mbar_arrive(smem_u32(&sm.turn[x ^ 1]));
           if (prev_vst >= 0) {
             mma_commit(smem_u32(&sm.v_empty[prev_vst]));
             if (++vst == Cfg::kVStages) { vst = 0; v_ph ^= 1; }
