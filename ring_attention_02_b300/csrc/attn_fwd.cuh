@@ -21,12 +21,14 @@
 //   warps 4..7   softmax of query tile A, one row per thread;
 //   warps 8..11  softmax of query tile B.
 // The two tiles run independent chains (S -> softmax -> P V -> next S).  The
-// issuers pass a turn back and forth (two mbarriers), so their batches
-// alternate on the tensor core: while one tile's softmax turns S into P, the
-// other tile's products run.  Measured on a B300 (32k causal forward): one
-// issuing thread 1041 TFLOP/s (its own barrier waits serialise both chains),
-// two free-running issuers 1111 (the chains fall into step, so both softmaxes
-// leave the tensor core idle together), two alternating issuers 1148.
+// issuers pass a turn back and forth (two mbarriers): an issuer takes the turn
+// before its P V and hands it on before its Q K^T, so the two chains stay half
+// a batch apart: one tile's softmax runs while the other tile's products do,
+// and the Q K^T of one overlaps the P V of the other at issue.  Measured on a
+// B300 (32k causal forward): one issuing thread 1041 TFLOP/s (its own barrier
+// waits serialise both chains), two free-running issuers 1111 (the chains fall
+// into step, so both softmaxes leave the tensor core idle together), turn
+// passed after each whole batch 1148, turn passed between P V and Q K^T 1250.
 //
 // Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D),
 // O_B [384,384+D).  P (bf16, two per column) overwrites the first 64 columns
@@ -65,6 +67,7 @@ struct FwdParams {
   float* lse;          // may be null
   unsigned long long* shard_tiles;  // may be null: per-shard count of multiplied tile pairs
   int64_t num_items;
+  int kv_group;        // (b, kv head) pairs per scheduling group (see unit_head)
 };
 
 template <int D>
@@ -100,15 +103,29 @@ struct UnitHead {
   int b, h, hkv, shard, seg, pair;
 };
 
+// Work items are ordered group-major: the (b, kv head) pairs are cut into
+// groups of p.kv_group, and a group's items all come before the next group's.
+// Inside a group the units come longest first, each with all its heads side by
+// side (the G query heads of one kv head adjacent).  With one group this is a
+// global longest-first order; smaller groups keep the key/value tiles the
+// running CTAs share inside L2 when all of them would not fit.
 __device__ __forceinline__ UnitHead unit_head(const FwdParams& p, int64_t item) {
   UnitHead u;
   const Geo& g = p.g;
-  const int bh_count = g.B * g.H;
-  const int bh = (int)(item % bh_count);
-  const int64_t unit = item / bh_count;
-  u.b = bh / g.H;
-  u.h = bh % g.H;
-  u.hkv = u.h / (g.H / g.Hkv);
+  const int G = g.H / g.Hkv;
+  const int BK = g.B * g.Hkv;
+  const int64_t U = units_total(g, p.mode == FWD_MODE_STEP);
+  const int64_t per_group = (int64_t)p.kv_group * G * U;
+  const int grp = (int)(item / per_group);
+  const int64_t rem = item % per_group;
+  const int left = BK - grp * p.kv_group;
+  const int hg = left < p.kv_group ? left : p.kv_group;   // pairs in this group
+  const int64_t unit = rem / ((int64_t)hg * G);
+  const int r2 = (int)(rem % ((int64_t)hg * G));
+  const int bk = grp * p.kv_group + r2 / G;
+  u.b = bk / g.Hkv;
+  u.hkv = bk % g.Hkv;
+  u.h = u.hkv * G + r2 % G;
   Unit w = unit_of(g, unit, p.mode == FWD_MODE_STEP, p.step_r);
   u.shard = w.shard;
   u.seg = w.seg;
@@ -340,10 +357,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               goto done;
             tc_fence_after();
           }
-          // Batches alternate between the two issuers (A, B, A, B, ...), so
-          // one tile's softmax runs while the tensor core works on the other
-          // tile's batch; left free, the two chains fall into step and both
-          // softmaxes then leave the tensor core idle at the same time.
+          // The turn alternates between the two issuers (A, B, A, B, ...) and
+          // is handed on between this issuer's P V and its Q K^T; left free,
+          // the two chains fall into step and both softmaxes then leave the
+          // tensor core idle at the same time.
           if (first_turn) {
             first_turn = false;
           } else {
@@ -367,6 +384,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             pend = false;
             if (cnt_pv == nx) mma_commit(smem_u32(&sm.o_full[x]));
           }
+          mbar_arrive(smem_u32(&sm.turn[x ^ 1]));
           if (more && act) {
             if (cnt_s == 0) {
               if (!mbar_wait(smem_u32(&sm.q_full[x]), q_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
@@ -388,7 +406,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (cnt_s == nx) mma_commit(smem_u32(&sm.q_empty[x]));
             pend = true;
           }
-          mbar_arrive(smem_u32(&sm.turn[x ^ 1]));
           if (prev_vst >= 0) {
             mma_commit(smem_u32(&sm.v_empty[prev_vst]));
             if (++vst == Cfg::kVStages) { vst = 0; v_ph ^= 1; }

@@ -40,6 +40,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct DeviceInfo {
   int sms = 0;
   int cc_major = 0;
+  int l2_bytes = 0;
   bool fwd_attr_set[2] = {false, false};
   bool bwd_attr_set[2] = {false, false};
 };
@@ -59,8 +60,12 @@ ra_status device_info(DeviceInfo** out) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
     e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(CC)");
+    int l2 = 0;
+    e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(L2 size)");
     d.sms = sms;
     d.cc_major = major;
+    d.l2_bytes = l2;
   }
   if (d.cc_major != 10)
     return fail(RA_ERR_UNSUPPORTED, "needs a Blackwell sm_10x GPU (found compute capability %d.x)",
@@ -156,6 +161,24 @@ ra_status launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   return RA_OK;
 }
 
+// (b, kv head) pairs per scheduling group of the forward.  One group (a global
+// longest-first order) unless the key/value tiles of all pairs would overflow
+// L2: then groups whose keys and values fit in about 3/4 of L2, as long as a
+// group still spans at least 8 rounds of the grid (fewer rounds would cost
+// more in load balance than the L2 hits gain).
+int fwd_kv_group(const ra::Geo& g, bool step, const DeviceInfo* dev, int D) {
+  const int BK = g.B * g.Hkv;
+  const int64_t kv_bytes_pair = (int64_t)(step ? g.n : g.S) * D * 2 * 2;
+  const int64_t budget = (int64_t)dev->l2_bytes * 3 / 4;
+  if (kv_bytes_pair * BK <= budget) return BK;
+  int64_t hg = budget / kv_bytes_pair;
+  if (hg < 1) hg = 1;
+  const int G = g.H / g.Hkv;
+  const int64_t items_per_group = hg * G * ra::units_total(g, step);
+  if (items_per_group < 8 * (int64_t)dev->sms) return BK;
+  return (int)(hg < BK ? hg : BK);
+}
+
 ra_status fwd_impl(int mode, const void* q, const void* k, const void* v, void* out, int out_f32,
                    float* lse, int B, int H, int Hkv, int64_t S, int D, int P, int layout,
                    int causal, float scale, int r, int s, unsigned long long* shard_tiles,
@@ -184,6 +207,7 @@ ra_status fwd_impl(int mode, const void* q, const void* k, const void* v, void* 
   prm.shard_tiles = shard_tiles;
   const bool step = mode == ra::FWD_MODE_STEP;
   prm.num_items = ra::units_total(prm.g, step) * B * H;
+  prm.kv_group = fwd_kv_group(prm.g, step, dev, D);
 
   CUtensorMap mq, mk, mv;
   const int64_t n = S / P;
