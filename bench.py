@@ -9,6 +9,12 @@ With a training workload (``--workload train-B2H16S32768D128P8``) one step
 is ``ring_attn_fwd`` followed by ``ring_attn_bwd`` (dq, dk, dv from a seeded
 dO), counted as 3.5x the forward's flops.
 
+``--op`` times one of the other calls on the workload's shapes instead:
+``permute`` (token rows of q into shard-major order, HBM bound), ``merge``
+(LSE fold of one shard's fp32 partials, HBM bound) or ``step_merge`` (the
+per-hop form of the whole ring: P*P ``ring_attn_step`` calls and the
+``ring_attn_merge`` folds, on shard-major inputs permuted beforehand).
+
 Prints one JSON line.  ``--impl reference`` times the CPU oracle instead
 (bounded samples of the same workload on the host cores).
 """
@@ -145,6 +151,14 @@ def measured_peaks():
             d = json.load(f)
         return d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "of measured"
     return 1800.0, 1400.0, "of fallback"
+
+
+def measured_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f).get("hbm_gbs"), "of measured"
+    return 6400.0, "of fallback"
 
 
 FWD_SOURCES = ["attn_fwd.cuh", "geometry.cuh", "sm103_ptx.cuh"]
@@ -419,6 +433,100 @@ def run_ours(args, w: Workload, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
+def run_op(args, w: Workload, rank: int, world: int):
+    """Times ring_attn_permute, ring_attn_merge or the step+merge ring on the
+    workload's shapes (device-resident inputs; CUDA events on the stream)."""
+    from ring_attention_02_b300 import api
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    n = w.S // w.P
+    q, k, v = make_for(w, seed=args.seed + 17 * rank, device=dev)
+    hbm_peak, hbm_src = measured_hbm()
+    launches_per_step = 1
+    if args.op == "permute":
+        dst = torch.empty_like(q)
+        step = lambda: api.permute(q, w.S, w.P, w.layout, out=dst, stream=stream)
+        work = 2.0 * q.numel() * q.element_size()          # bytes read + written
+        unit, bound, peak, peak_src = "GB/s", "hbm", hbm_peak, hbm_src
+        metric = "ring_attn_permute HBM GB/s (q rows to shard-major order)"
+        dtype = "u8"
+    elif args.op == "merge":
+        g = torch.Generator(device=dev).manual_seed(args.seed + 5)
+        oa = torch.randn((w.B, n, w.H, w.D), device=dev, generator=g)
+        op = torch.randn((w.B, n, w.H, w.D), device=dev, generator=g)
+        la = torch.randn((w.B, w.H, n), device=dev, generator=g)
+        lp = torch.randn((w.B, w.H, n), device=dev, generator=g)
+        step = lambda: api.merge(oa, la, op, lp, stream=stream)
+        rows = w.B * n * w.H
+        work = 3.0 * rows * (4 * w.D + 4)                   # read both partials, write one
+        unit, bound, peak, peak_src = "GB/s", "hbm", hbm_peak, hbm_src
+        metric = "ring_attn_merge HBM GB/s (LSE fold of one shard's fp32 partials)"
+        dtype = "f32"
+    else:
+        qs = api.permute(q, w.S, w.P, w.layout).view(w.B, w.P, n, w.H, w.D)
+        ks = api.permute(k, w.S, w.P, w.layout).view(w.B, w.P, n, w.Hkv, w.D)
+        vs = api.permute(v, w.S, w.P, w.layout).view(w.B, w.P, n, w.Hkv, w.D)
+        qs = [qs[:, r].contiguous() for r in range(w.P)]
+        ks = [ks[:, r].contiguous() for r in range(w.P)]
+        vs = [vs[:, r].contiguous() for r in range(w.P)]
+        acc_o = torch.empty((w.B, n, w.H, w.D), dtype=torch.float32, device=dev)
+        acc_l = torch.empty((w.B, w.H, n), dtype=torch.float32, device=dev)
+        part_o, part_l = torch.empty_like(acc_o), torch.empty_like(acc_l)
+
+        def step():
+            for r in range(w.P):
+                api.step(qs[r], ks[r], vs[r], w.S, w.P, w.layout, r, r, w.causal, out=acc_o,
+                         lse=acc_l, stream=stream)
+                for t in range(1, w.P):
+                    s_blk = (r - t) % w.P
+                    api.step(qs[r], ks[s_blk], vs[s_blk], w.S, w.P, w.layout, r, s_blk,
+                             w.causal, out=part_o, lse=part_l, stream=stream)
+                    api.merge(acc_o, acc_l, part_o, part_l, stream=stream)
+        work = w.counted_flops()
+        unit, bound = UNIT, "tensor"
+        peak, _, peak_src = measured_peaks()
+        metric = "causal ring-attn step+merge ring TFLOP/s (bf16, per-hop calls, 1 B300)"
+        dtype = "bf16"
+        launches_per_step = w.P * w.P + w.P * (w.P - 1)
+    for _ in range(args.warmup):
+        step()
+    api.check_status(stream)
+    _barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    _barrier()
+    api.check_status(stream)
+    ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
+    scale = 1e9 if unit == "GB/s" else 1e12
+    value = world * work / (ms * 1e-3) / scale
+    if rank != 0:
+        return
+    achieved = work / (ms * 1e-3) / scale
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+        "config": {**config_of(w), "op": args.op},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+                     "work_per_launch": work},
+        "cpu_baseline": None,
+        "e2e": None,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -435,6 +543,8 @@ def main(argv=None):
     ap.add_argument("--ref-prefix", type=int, default=12288,
                     help="training workloads: tokens of the oracle's fwd+bwd sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["fwd", "permute", "merge", "step_merge"], default="fwd",
+                    help="fwd: the workload's step (default); the others time one call")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -444,6 +554,8 @@ def main(argv=None):
     rank, world = _dist()
     if args.impl == "reference":
         run_reference(args, w, rank)
+    elif args.op != "fwd":
+        run_op(args, w, rank, world)
     else:
         run_ours(args, w, rank, world)
     if torch.distributed.is_available() and torch.distributed.is_initialized():

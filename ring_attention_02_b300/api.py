@@ -170,14 +170,17 @@ def bwd_noalloc(q, k, v, out, lse, dout, P: int, layout, causal: bool = True,
 
 
 def step(q_shard, k_shard, v_shard, S: int, P: int, layout, r: int, s: int,
-         causal: bool = True, scale: float | None = None, stream=None):
-    """One ring hop in shard-local order: (out_part fp32 [B,n,H,D], lse_part [B,H,n])."""
+         causal: bool = True, scale: float | None = None, out=None, lse=None, stream=None):
+    """One ring hop in shard-local order: (out_part fp32 [B,n,H,D], lse_part [B,H,n]),
+    written into `out` and `lse` when given."""
     B, n, H, D = q_shard.shape
     Hkv = k_shard.shape[2]
     if scale is None:
         scale = D ** -0.5
-    out = torch.empty((B, n, H, D), dtype=torch.float32, device=q_shard.device)
-    lse = torch.empty((B, H, n), dtype=torch.float32, device=q_shard.device)
+    if out is None:
+        out = torch.empty((B, n, H, D), dtype=torch.float32, device=q_shard.device)
+    if lse is None:
+        lse = torch.empty((B, H, n), dtype=torch.float32, device=q_shard.device)
     _check(lib().ring_attn_step(_ptr(q_shard), _ptr(k_shard), _ptr(v_shard), _ptr(out),
                                 _ptr(lse), B, H, Hkv, S, D, P, _layout(layout), r, s,
                                 int(bool(causal)), float(scale), _stream(stream)))
