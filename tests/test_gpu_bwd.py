@@ -43,6 +43,8 @@ def _compare(q, k, v, do, dq, dk, dv, causal, scale, pairs):
     errs = {}
     for name, ours, ref in (("dq", ours_q, rq), ("dk", ours_k, rk), ("dv", ours_v, rv)):
         errs[name] = (max_abs(ours, ref), rel_l2(ours, ref))
+    print(f"PARITY bwd B{q.shape[0]} S{q.shape[1]} H{H} Hkv{Hkv} D{q.shape[3]} pairs={pairs}: "
+          + " ".join(f"{n} max|d|={a:.3e} relL2={r:.3e}" for n, (a, r) in errs.items()))
     for name, (ea, er) in errs.items():
         assert ea <= ABS_TOL and er <= REL_TOL, (name, errs)
     return errs

@@ -28,6 +28,8 @@ def _check_full(q, k, v, P, layout, causal, out_dtype=torch.bfloat16, scale=None
     api.check_status()
     ro, rl = oracle.attn_fwd(to64(q), to64(k), to64(v), causal, scale)
     eo, el = max_abs(to64(out), ro), max_abs(to64(lse), rl)
+    print(f"PARITY fwd B{q.shape[0]} S{q.shape[1]} H{q.shape[2]} Hkv{k.shape[2]} D{D} P{P} "
+          f"{layout} causal={causal}: max|out|={eo:.3e} max|lse|={el:.3e}")
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
     return eo, el
 
@@ -90,7 +92,10 @@ def _sampled(w, layout, rows_count, seed=0):
     rows = sample_rows(w.S, w.P, layout, rows_count, seed=seed)
     ridx = torch.from_numpy(rows).cuda()
     ro, rl = oracle.attn_fwd_rows(to64(q[:, ridx]), rows, to64(k), to64(v), w.causal, w.scale)
-    return max_abs(to64(out[:, ridx]), ro), max_abs(to64(lse[:, :, ridx]), rl)
+    eo, el = max_abs(to64(out[:, ridx]), ro), max_abs(to64(lse[:, :, ridx]), rl)
+    print(f"PARITY fwd {w.name} {layout} ({len(rows)} sampled rows): max|out|={eo:.3e} "
+          f"max|lse|={el:.3e}")
+    return eo, el
 
 
 @pytest.mark.parametrize("layout", ["striped", "zigzag"])
