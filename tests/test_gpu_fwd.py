@@ -10,7 +10,8 @@ import torch
 
 import oracle
 from ring_attention_02_b300 import api
-from ring_attention_02_b300.inputs import (CAUSAL_8K, GQA_128K, MILLION, TINY, make_qkv)
+from ring_attention_02_b300.inputs import (CAUSAL_8K, GQA_128K, MILLION, TINY, TRAIN_32K,
+                                           make_qkv)
 
 from helpers import max_abs, sample_rows, to64
 
@@ -106,6 +107,12 @@ def test_gqa_128k_sampled(layout):
 
 def test_million_token_sampled():
     eo, el = _sampled(MILLION, "zigzag", 24)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+def test_training_workload_forward_sampled():
+    # the forward half of the training step (B=2, H=16, S=32768, zig-zag)
+    eo, el = _sampled(TRAIN_32K, "zigzag", 32)
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
 
 
