@@ -355,6 +355,80 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
         pack_bf16x2(__uint_as_float(r[8 * i + 6]) * mul, __uint_as_float(r[8 * i + 7]) * mul));
 }
 
+// dK/dV pass, one half of a tile, one key row per thread: reads S^T and dP^T
+// (64 query columns starting at col0 of the tile), writes P^T and dS^T as bf16
+// over the first half of their regions.  Query columns below `lo` precede the
+// key and are masked out (kMasked only).
+template <bool kMasked>
+__device__ __forceinline__ void dkdv_half(uint32_t t_s, uint32_t t_dp, const float* nl,
+                                          const float* nd, float2 sl2, int lo, int col0) {
+#pragma unroll
+  for (int c2 = 0; c2 < 2; ++c2) {
+    uint32_t s[32], dp[32];
+    tmem_ld32(t_s + 32 * c2, s);
+    tmem_ld32(t_dp + 32 * c2, dp);
+    tmem_wait_ld();
+    uint32_t pk_p[16], pk_ds[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      const float4 nl4 = *reinterpret_cast<const float4*>(nl + 32 * c2 + i);
+      const float4 nd4 = *reinterpret_cast<const float4*>(nd + 32 * c2 + i);
+#pragma unroll
+      for (int j = 0; j < 4; j += 2) {
+        const float2 nlj = j == 0 ? make_float2(nl4.x, nl4.y) : make_float2(nl4.z, nl4.w);
+        const float2 ndj = j == 0 ? make_float2(nd4.x, nd4.y) : make_float2(nd4.z, nd4.w);
+        const float2 t2 = fma2(make_float2(__uint_as_float(s[i + j]),
+                                           __uint_as_float(s[i + j + 1])), sl2, nlj);
+        float p0 = ex2_approx(t2.x), p1 = ex2_approx(t2.y);
+        if (kMasked) {
+          const int qc = col0 + 32 * c2 + i + j;   // query column within the tile
+          p0 = qc < lo ? 0.f : p0;
+          p1 = qc + 1 < lo ? 0.f : p1;
+        }
+        const float2 dd = add2(make_float2(__uint_as_float(dp[i + j]),
+                                           __uint_as_float(dp[i + j + 1])), ndj);
+        const float2 ds = mul2(make_float2(p0, p1), dd);
+        pk_p[(i + j) / 2] = pack_bf16x2(p0, p1);
+        pk_ds[(i + j) / 2] = pack_bf16x2(ds.x, ds.y);
+      }
+    }
+    tmem_st16(t_s + 16 * c2, pk_p);
+    tmem_st16(t_dp + 16 * c2, pk_ds);
+  }
+}
+
+// dQ pass, one half of a tile, one query row per thread: reads S and dP (64
+// key columns starting at col0), writes dS as bf16 over the first half of the
+// S region.  Key columns at or beyond `lim` are masked out (kMasked only).
+template <bool kMasked>
+__device__ __forceinline__ void dq_half(uint32_t t_s, uint32_t t_dp, float2 sl2, float2 nl2,
+                                        float2 nd2, int lim, int col0) {
+#pragma unroll
+  for (int c2 = 0; c2 < 2; ++c2) {
+    uint32_t s[32], dp[32];
+    tmem_ld32(t_s + 32 * c2, s);
+    tmem_ld32(t_dp + 32 * c2, dp);
+    tmem_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float2 t2 = fma2(make_float2(__uint_as_float(s[i]), __uint_as_float(s[i + 1])),
+                             sl2, nl2);
+      float p0 = ex2_approx(t2.x), p1 = ex2_approx(t2.y);
+      if (kMasked) {
+        const int kc = col0 + 32 * c2 + i;   // key column within the tile
+        p0 = kc < lim ? p0 : 0.f;
+        p1 = kc + 1 < lim ? p1 : 0.f;
+      }
+      const float2 dd = add2(make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])),
+                             nd2);
+      const float2 ds = mul2(make_float2(p0, p1), dd);
+      pk[i / 2] = pack_bf16x2(ds.x, ds.y);
+    }
+    tmem_st16(t_s + 16 * c2, pk);
+  }
+}
+
 // ---------------------------------------------------------------- dK / dV pass
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -551,6 +625,15 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       if (!kt.valid || !qiter_next(g, it)) continue;
       const int kpos = kt.pos0 + kt.stride * (kt.off + row);
       do {
+        // The tile's geometry does not depend on S: work it out while the
+        // products are still running.
+        const QTile qt = make_qtile(g, it.r, it.sq, it.a);
+        int lo = 0;   // query columns below lo precede this key: masked out
+        if (g.causal && qt.qmin < kt.qmax) {
+          const int cnt = count_le(it.seg, kpos - 1) - qt.off;
+          lo = cnt < 0 ? 0 : (cnt > kTile ? kTile : cnt);
+        }
+        const bool masked = __any_sync(0xffffffffu, lo > 64 * x);
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[x]), s_ph,
                                                RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
           goto done;
@@ -559,46 +642,12 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                                                RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
           goto done;
         tc_fence_after();
-        const QTile qt = make_qtile(g, it.r, it.sq, it.a);
-        // query columns below `lo` precede this key: masked out
-        int lo = 0;
-        if (g.causal && qt.qmin < kt.qmax) {
-          const int cnt = count_le(it.seg, kpos - 1) - qt.off;
-          lo = cnt < 0 ? 0 : (cnt > kTile ? kTile : cnt);
-        }
         const float* nl = sm.nlse2[st] + 64 * x;
         const float* nd = sm.ndelta[st] + 64 * x;
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t s[32], dp[32];
-          tmem_ld32(t_s + 32 * c2, s);
-          tmem_ld32(t_dp + 32 * c2, dp);
-          tmem_wait_ld();
-          uint32_t pk_p[16], pk_ds[16];
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 nl4 = *reinterpret_cast<const float4*>(nl + 32 * c2 + i);
-            const float4 nd4 = *reinterpret_cast<const float4*>(nd + 32 * c2 + i);
-#pragma unroll
-            for (int j = 0; j < 4; j += 2) {
-              const int qc = 64 * x + 32 * c2 + i + j;   // query column within the tile
-              const float2 nlj = j == 0 ? make_float2(nl4.x, nl4.y) : make_float2(nl4.z, nl4.w);
-              const float2 ndj = j == 0 ? make_float2(nd4.x, nd4.y) : make_float2(nd4.z, nd4.w);
-              const float2 t2 = fma2(make_float2(__uint_as_float(s[i + j]),
-                                                 __uint_as_float(s[i + j + 1])), sl2, nlj);
-              float p0 = ex2_approx(t2.x), p1 = ex2_approx(t2.y);
-              p0 = qc < lo ? 0.f : p0;
-              p1 = qc + 1 < lo ? 0.f : p1;
-              const float2 dd = add2(make_float2(__uint_as_float(dp[i + j]),
-                                                 __uint_as_float(dp[i + j + 1])), ndj);
-              const float2 ds = mul2(make_float2(p0, p1), dd);
-              pk_p[(i + j) / 2] = pack_bf16x2(p0, p1);
-              pk_ds[(i + j) / 2] = pack_bf16x2(ds.x, ds.y);
-            }
-          }
-          tmem_st16(t_s + 16 * c2, pk_p);
-          tmem_st16(t_dp + 16 * c2, pk_ds);
-        }
+        if (masked)
+          dkdv_half<true>(t_s, t_dp, nl, nd, sl2, lo, 64 * x);
+        else
+          dkdv_half<false>(t_s, t_dp, nl, nd, sl2, lo, 64 * x);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.p_full[x]));
@@ -856,33 +905,16 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           const int cl = count_le(it.seg, qpos) - k0;
           lim = cl < 0 ? 0 : (cl > kvalid ? kvalid : cl);
         }
+        const bool masked = __any_sync(0xffffffffu, lim < 64 * x + 64);
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[x]), s_ph,
                                                RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
           goto done;
         s_ph ^= 1;
         tc_fence_after();
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t s[32], dp[32];
-          tmem_ld32(t_s + 32 * c2, s);
-          tmem_ld32(t_dp + 32 * c2, dp);
-          tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int kc = 64 * x + 32 * c2 + i;   // key column within the tile
-            const float2 t2 = fma2(make_float2(__uint_as_float(s[i]), __uint_as_float(s[i + 1])),
-                                   sl2_2, nl2);
-            float p0 = ex2_approx(t2.x), p1 = ex2_approx(t2.y);
-            p0 = kc < lim ? p0 : 0.f;
-            p1 = kc + 1 < lim ? p1 : 0.f;
-            const float2 dd = add2(make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])),
-                                   nd2);
-            const float2 ds = mul2(make_float2(p0, p1), dd);
-            pk[i / 2] = pack_bf16x2(ds.x, ds.y);
-          }
-          tmem_st16(t_s + 16 * c2, pk);
-        }
+        if (masked)
+          dq_half<true>(t_s, t_dp, sl2_2, nl2, nd2, lim, 64 * x);
+        else
+          dq_half<false>(t_s, t_dp, sl2_2, nl2, nd2, lim, 64 * x);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.p_full[x]));
