@@ -11,9 +11,11 @@ dO), counted as 3.5x the forward's flops.
 
 ``--op`` times one of the other calls on the workload's shapes instead:
 ``permute`` (token rows of q into shard-major order, HBM bound), ``merge``
-(LSE fold of one shard's fp32 partials, HBM bound) or ``step_merge`` (the
+(LSE fold of one shard's fp32 partials, HBM bound), ``step_merge`` (the
 per-hop form of the whole ring: P*P ``ring_attn_step`` calls and the
-``ring_attn_merge`` folds, on shard-major inputs permuted beforehand).
+``ring_attn_merge`` folds, on shard-major inputs permuted beforehand) or
+``decode`` (``--decode-tokens`` new tokens against the workload's key/value
+cache, HBM bound).
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle instead
 (bounded samples of the same workload on the host cores).
@@ -465,6 +467,17 @@ def run_op(args, w: Workload, rank: int, world: int):
         unit, bound, peak, peak_src = "GB/s", "hbm", hbm_peak, hbm_src
         metric = "ring_attn_merge HBM GB/s (LSE fold of one shard's fp32 partials)"
         dtype = "f32"
+    elif args.op == "decode":
+        T = args.decode_tokens
+        qd = q[:, w.S - T:].contiguous()
+        out_d = torch.empty_like(qd)
+        lse_d = torch.empty((w.B, w.H, T), dtype=torch.float32, device=dev)
+        step = lambda: api.decode(qd, k, v, w.P, w.layout, out=out_d, lse=lse_d, stream=stream)
+        work = 2.0 * k.numel() * k.element_size()             # the cache is read once per step
+        unit, bound, peak, peak_src = "GB/s", "hbm", hbm_peak, hbm_src
+        metric = f"ring_attn_decode HBM GB/s ({T} new token(s) against the sharded cache)"
+        dtype = "bf16"
+        launches_per_step = 2
     else:
         qs = api.permute(q, w.S, w.P, w.layout).view(w.B, w.P, n, w.H, w.D)
         ks = api.permute(k, w.S, w.P, w.layout).view(w.B, w.P, n, w.Hkv, w.D)
@@ -543,7 +556,9 @@ def main(argv=None):
     ap.add_argument("--ref-prefix", type=int, default=12288,
                     help="training workloads: tokens of the oracle's fwd+bwd sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["fwd", "permute", "merge", "step_merge"], default="fwd",
+    ap.add_argument("--decode-tokens", type=int, default=1, help="--op decode: new tokens T")
+    ap.add_argument("--op", choices=["fwd", "permute", "merge", "step_merge", "decode"],
+                    default="fwd",
                     help="fwd: the workload's step (default); the others time one call")
     args = ap.parse_args(argv)
     if args.warmup < 3:

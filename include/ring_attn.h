@@ -161,6 +161,31 @@ ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
                                 int causal, float scale, void* stream);
 
 /*
+ * ring_attn_decode -- inference step against a sharded key/value cache.  The
+ * pages put ring attention to work on ultra-long-context inference
+ * ("Sequenzparallelitaet und Ringaufmerksamkeit", "Die Zukunft ..." and its
+ * use cases), with the history's keys and values kept in a cache and read
+ * back rather than recomputed (the Chinese article on long-context
+ * inference).  T new query tokens at positions S-T .. S-1 attend to the S
+ * cached tokens (their own keys and values already appended): query t sees
+ * the keys at positions <= S-T+t.  The P ranks of the ring hold the cache by
+ * `layout`; each computes a partial over the keys it holds, and the partials
+ * are merged as in ring_attn_merge.  Equal to ring_attn_fwd's rows S-T .. S-1.
+ *   q        [B][T][H][D] bf16
+ *   k_cache, v_cache  [B][S][Hkv][D] bf16, natural token order
+ *   out      [B][T][H][D], bf16 (RA_BF16) or fp32 (RA_F32)
+ *   lse      [B][H][T] fp32, or NULL
+ * Needs (H/Hkv) * T <= 16 and 1 <= T <= S, plus ring_attn_fwd's size rules.
+ * The step reads the whole cache once: it is bound by HBM bandwidth and runs
+ * on the CUDA cores.  Takes a transient fp32 workspace for the partials with
+ * cudaMallocAsync / cudaFreeAsync on `stream`; returns RA_ERR_ALLOC if that
+ * fails.
+ */
+ra_status ring_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out,
+                           ra_dtype out_dtype, float* lse, int B, int H, int Hkv, int T, int64_t S,
+                           int D, int P, ra_layout layout, float scale, void* stream);
+
+/*
  * ring_attn_step -- one ring hop: the queries of shard r against the key/value
  * block of shard s only ("Tiefer Einblick": as each block arrives the GPU
  * computes a partial attention), causal on global positions, normalised

@@ -49,6 +49,8 @@ def lib() -> ctypes.CDLL:
             L.ring_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64,
                                         i32, i32, i32, i32, f32, vp]
             L.ring_attn_bwd_noalloc.argtypes = L.ring_attn_bwd.argtypes
+            L.ring_attn_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64,
+                                           i32, i32, i32, f32, vp]
             L.ring_attn_step.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, i32, i32,
                                          i32, i32, i32, f32, vp]
             L.ring_attn_merge.argtypes = [vp, vp, vp, vp, i32, i32, i64, i32, vp]
@@ -59,7 +61,7 @@ def lib() -> ctypes.CDLL:
             L.ring_attn_last_error.restype = ctypes.c_char_p
             L.ring_attn_version.restype = ctypes.c_char_p
             for name in ("ring_attn_fwd", "ring_attn_fwd_counted", "ring_attn_bwd",
-                         "ring_attn_bwd_noalloc",
+                         "ring_attn_bwd_noalloc", "ring_attn_decode",
                          "ring_attn_step", "ring_attn_merge", "ring_attn_permute",
                          "ring_attn_index_map", "ring_attn_census", "ring_attn_check_status"):
                 getattr(L, name).restype = ctypes.c_int
@@ -167,6 +169,29 @@ def bwd_noalloc(q, k, v, out, lse, dout, P: int, layout, causal: bool = True,
                                        D, P, _layout(layout), int(bool(causal)), float(scale),
                                        _stream(stream)))
     return dq, dk, dv
+
+
+def decode(q, k_cache, v_cache, P: int, layout, scale: float | None = None,
+           out_dtype=torch.bfloat16, out=None, lse=None, want_lse: bool = True, stream=None):
+    """Decode step: q [B,T,H,D] (positions S-T..S-1) against caches [B,S,Hkv,D].
+
+    Returns (out [B,T,H,D] in out_dtype, lse [B,H,T] fp32 or None).
+    """
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, nm)
+    B, T, H, D = q.shape
+    S, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, T, H, D), dtype=out_dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    odt = RA_F32 if out.dtype == torch.float32 else RA_BF16
+    _check(lib().ring_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), odt,
+                                  _ptr(lse), B, H, Hkv, T, S, D, P, _layout(layout),
+                                  float(scale), _stream(stream)))
+    return out, lse
 
 
 def step(q_shard, k_shard, v_shard, S: int, P: int, layout, r: int, s: int,

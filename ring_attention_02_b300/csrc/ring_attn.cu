@@ -13,6 +13,7 @@
 
 #include "../../include/ring_attn.h"
 #include "attn_bwd.cuh"
+#include "attn_decode.cuh"
 #include "attn_fwd.cuh"
 #include "elementwise.cuh"
 #include "geometry.cuh"
@@ -43,6 +44,7 @@ struct DeviceInfo {
   int l2_bytes = 0;
   bool fwd_attr_set[2] = {false, false};
   bool bwd_attr_set[2] = {false, false};
+  bool dec_attr_set[2] = {false, false};
 };
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
@@ -356,6 +358,32 @@ ra_status fixed_workspace(float** out) {
   return RA_OK;
 }
 
+// ---------------------------------------------------------------- decode
+template <int D>
+ra_status launch_decode_d(const CUtensorMap& mk, const CUtensorMap& mv, const ra::DecodeParams& prm,
+                          void* out, int out_f32, float* lse, DeviceInfo* dev,
+                          cudaStream_t stream) {
+  const size_t smem = sizeof(ra::DecodeSmem<D>) + 1024;
+  const int di = D == 128 ? 1 : 0;
+  if (!dev->dec_attr_set[di]) {
+    cudaError_t e = cudaFuncSetAttribute(ra::decode_partial_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode smem)");
+    dev->dec_attr_set[di] = true;
+  }
+  const ra::Geo& g = prm.g;
+  dim3 grid((unsigned)prm.chunks, (unsigned)(g.B * g.Hkv));
+  ra::decode_partial_kernel<D><<<grid, ra::kDecodeThreads, smem, stream>>>(mk, mv, prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "decode_partial_kernel launch");
+  const int64_t items = (int64_t)g.B * g.Hkv * prm.rows;
+  ra::decode_combine_kernel<D><<<(unsigned)items, 256, 0, stream>>>(
+      prm.part_o, prm.part_lse, out, out_f32, lse, g, prm.T, prm.rows, prm.chunks);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "decode_combine_kernel launch");
+  return RA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -435,6 +463,74 @@ ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   st = fixed_workspace(&ws);
   if (st != RA_OK) return st;
   return bwd_launch(a, ws, ws + kFixedVecMax, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out,
+                           ra_dtype out_dtype, float* lse, int B, int H, int Hkv, int T, int64_t S,
+                           int D, int P, ra_layout layout, float scale, void* stream) {
+  if (!q || !k_cache || !v_cache || !out)
+    return fail(RA_ERR_NULL, "q, k_cache, v_cache and out must be non-NULL");
+  if (out_dtype != RA_BF16 && out_dtype != RA_F32)
+    return fail(RA_ERR_UNSUPPORTED, "out_dtype %d", (int)out_dtype);
+  ra_status st = check_common(B, H, Hkv, S, D, P, (int)layout, scale);
+  if (st != RA_OK) return st;
+  if (T < 1 || T > S) return fail(RA_ERR_SHAPE, "T=%d new tokens must be in [1, S=%lld]", T, (long long)S);
+  if ((H / Hkv) * T > ra::kDecodeMaxRows)
+    return fail(RA_ERR_UNSUPPORTED, "(H/Hkv)*T = %d query rows per kv head; at most %d",
+                (H / Hkv) * T, ra::kDecodeMaxRows);
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return fail(RA_ERR_ALIGN, "q, k_cache, v_cache and out must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(RA_ERR_ALIGN, "lse must be 4-byte aligned");
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != RA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+  ra::DecodeParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.g = ra::make_geo(B, H, Hkv, S, P, (int)layout, 1);
+  const ra::Geo& g = prm.g;
+  prm.T = T;
+  prm.rows = (H / Hkv) * T;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  // Chunks of a shard segment's 128-slot tiles: about two CTAs per SM in all.
+  const int64_t tiles = (int64_t)B * Hkv * P * g.nseg * g.ntile;
+  int64_t ct = (tiles + 2 * dev->sms - 1) / (2 * (int64_t)dev->sms);
+  if (ct < 1) ct = 1;
+  if (ct > g.ntile) ct = g.ntile;
+  const int64_t per_seg = (g.ntile + ct - 1) / ct;
+  ct = (g.ntile + per_seg - 1) / per_seg;        // even out the chunks of a segment
+  prm.chunk_tiles = (int)ct;
+  prm.chunks_per_seg = (g.ntile + prm.chunk_tiles - 1) / prm.chunk_tiles;
+  prm.chunks = P * g.nseg * prm.chunks_per_seg;
+
+  const size_t n_lse = (size_t)B * Hkv * prm.chunks * prm.rows;
+  const size_t bytes = n_lse * sizeof(float) * (size_t)(D + 1);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, bytes, cs);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(RA_ERR_ALLOC, "cudaMallocAsync(%zu bytes) for decode partials: %s", bytes,
+                cudaGetErrorString(e));
+  }
+  prm.part_o = static_cast<float*>(ws);
+  prm.part_lse = prm.part_o + n_lse * D;
+
+  CUtensorMap mk, mv;
+  const int64_t n = S / P;
+  const bool striped = layout == RA_LAYOUT_STRIPED;
+  const int64_t phases = striped ? P : 1;
+  const int64_t rows = striped ? (int64_t)B * n : (int64_t)B * S;
+  st = make_token_map(&mk, k_cache, D, Hkv, phases, rows);
+  if (st == RA_OK) st = make_token_map(&mv, v_cache, D, Hkv, phases, rows);
+  if (st == RA_OK)
+    st = D == 128 ? launch_decode_d<128>(mk, mv, prm, out, out_dtype == RA_F32, lse, dev, cs)
+                  : launch_decode_d<64>(mk, mv, prm, out, out_dtype == RA_F32, lse, dev, cs);
+  e = cudaFreeAsync(ws, cs);
+  if (st != RA_OK) return st;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(decode partials)");
+  return RA_OK;
 }
 
 ra_status ring_attn_step(const void* q_shard, const void* k_shard, const void* v_shard,
