@@ -316,14 +316,17 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
 }
 
 // out[b][t][h][:] and lse[b][h][t] from the partials of row i = e*T + t of
-// (b, kv head), h = hkv*G + e: one CTA (8 warps) per row; the warps split the
-// partials, first for the maximum lse, then for the weighted sum.
+// (b, kv head), h = hkv*G + e: one CTA (16 warps) per row; the warps split the
+// partials, first for the maximum lse, then for the weighted sum (unrolled so
+// several partials' loads are in flight per warp).
+constexpr int kCombineWarps = 16;
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCombineWarps * 32)
 decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                       void* out, int out_f32, float* lse, Geo g, int T, int rows, int chunks) {
   constexpr int kPer = D / 32;
-  __shared__ float red[8][D + 2];
+  __shared__ float red[kCombineWarps][D + 2];
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   const int item = blockIdx.x;                 // (bk, i)
   const int i = item % rows, bk = item / rows;
@@ -336,12 +339,13 @@ decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict_
   __syncthreads();
   float M = -INFINITY;
 #pragma unroll
-  for (int w2 = 0; w2 < 8; ++w2) M = fmaxf(M, red[w2][D]);
+  for (int w2 = 0; w2 < kCombineWarps; ++w2) M = fmaxf(M, red[w2][D]);
   float acc[kPer], s = 0.f;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
   if (M != -INFINITY) {
-    for (int c = warp; c < chunks; c += 8) {
+#pragma unroll 4
+    for (int c = warp; c < chunks; c += kCombineWarps) {
       const int64_t pi = pbase + (int64_t)c * rows;
       const float l = __ldg(part_lse + pi);
       const float w = l == -INFINITY ? 0.f : expf(l - M);
@@ -359,7 +363,7 @@ decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict_
   if (warp == 0) {
     float S = 0.f;
 #pragma unroll
-    for (int w2 = 0; w2 < 8; ++w2) S += red[w2][D + 1];
+    for (int w2 = 0; w2 < kCombineWarps; ++w2) S += red[w2][D + 1];
     const int b = bk / g.Hkv, hkv = bk % g.Hkv;
     const int G = g.H / g.Hkv;
     const int e = i / T, t = i % T;
@@ -370,7 +374,7 @@ decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict_
     for (int j = 0; j < kPer; ++j) {
       float v = 0.f;
 #pragma unroll
-      for (int w2 = 0; w2 < 8; ++w2) v += red[w2][lane + 32 * j];
+      for (int w2 = 0; w2 < kCombineWarps; ++w2) v += red[w2][lane + 32 * j];
       v *= inv;
       if (out_f32)
         static_cast<float*>(out)[orow * D + lane + 32 * j] = v;

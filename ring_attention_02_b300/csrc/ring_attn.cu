@@ -377,7 +377,7 @@ ra_status launch_decode_d(const CUtensorMap& mk, const CUtensorMap& mv, const ra
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode_partial_kernel launch");
   const int64_t items = (int64_t)g.B * g.Hkv * prm.rows;
-  ra::decode_combine_kernel<D><<<(unsigned)items, 256, 0, stream>>>(
+  ra::decode_combine_kernel<D><<<(unsigned)items, ra::kCombineWarps * 32, 0, stream>>>(
       prm.part_o, prm.part_lse, out, out_f32, lse, g, prm.T, prm.rows, prm.chunks);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode_combine_kernel launch");
