@@ -36,8 +36,9 @@
 // Q K^T into that region is issued after the P V that reads it, and tcgen05
 // MMAs of one thread execute in issue order.
 //
-// Lazy rescaling: a row keeps its running maximum until a tile raises it by
-// more than 8 (log2 units); P entries then stay below 2^8, and the final O / l
+// Lazy rescaling: a row keeps its running maximum until a tile's exponentials
+// against it sum above 2^12 (the exact pass then raises the maximum, with a
+// slack of 8 in log2 units); P entries stay below 2^12, and the final O / l
 // uses the same maximum in numerator and denominator, so the result is exact.
 #pragma once
 #include "geometry.cuh"
@@ -480,21 +481,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           float2 sum2 = make_float2(0.f, 0.f);
           bool done_p = false;
           if (!masked && pos_scale && m_run != -INFINITY) {
-            // Speculative pass: exponentials against the running max while the
-            // tile max is gathered alongside.  Valid unless this tile raises the
-            // max by more than 8 (then redone below), since P then stays < 2^8.
+            // Speculative pass: exponentials against the running max, without
+            // the tile max.  The tile's sum bounds its largest entry, so it is
+            // kept when that sum stays <= 2^12 (entries <= 2^12: harmless in bf16
+            // P and fp32 O, and O / l uses one max for both); otherwise the
+            // exact pass below redoes the tile with the max updated.
             const float2 sl2_2 = make_float2(sl2, sl2);
             const float2 negm2 = make_float2(-m_run, -m_run);
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int cch = 0; cch < 4; ++cch) {
               uint32_t pk[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 const int c0 = cch * 32 + 2 * i;
-                mx[i % 4] = max3f(mx[i % 4], s[c0], s[c0 + 1]);
                 const float2 t2 = fma2(make_float2(s[c0], s[c0 + 1]), sl2_2, negm2);
                 const float p0 = ex2_approx(t2.x);
                 const float p1 = ex2_approx(t2.y);
@@ -503,10 +504,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               }
               tmem_st16(t_s + cch * 16, pk);
             }
-            const float m_tile = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
-            const bool ok = !(m_tile > m_run + 8.f);
+            const float2 sum_t = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+            const bool ok = sum_t.x + sum_t.y <= 4096.f;
             if (__all_sync(0xffffffffu, ok)) {
-              sum2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+              sum2 = sum_t;
               done_p = true;
             }
           }
