@@ -110,6 +110,16 @@ def test_million_token_sampled():
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
 
 
+def test_l2_scheduling_groups_with_a_partial_last_group():
+    # 3 kv heads of 46 MB of keys and values each overflow L2, so the forward
+    # schedules them in groups of two (the last group holds one); checked on
+    # sampled rows of every head
+    from ring_attention_02_b300.inputs import Workload
+    w = Workload("gqa-B1H9Hkv3S90112D128P16", 1, 9, 3, 90112, 128, 16, "zigzag", True)
+    eo, el = _sampled(w, "zigzag", 24)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
 def test_training_workload_forward_sampled():
     # the forward half of the training step (B=2, H=16, S=32768, zig-zag)
     eo, el = _sampled(TRAIN_32K, "zigzag", 32)
