@@ -248,6 +248,18 @@ ra_status ring_attn_census(int64_t S, int P, ra_layout layout, int causal,
  */
 ra_status ring_attn_check_status(void* stream);
 
+/*
+ * ring_attn_wait_selfcheck -- exercises the failure path every kernel's waits
+ * share, without a fault: one thread waits on a barrier that nothing ever
+ * completes, gives up after limit_ms (1..1000) milliseconds, records a timeout
+ * in the device status word and returns; the context stays usable.  The next
+ * ring_attn_check_status() then reports RA_ERR_DEVICE_TIMEOUT and clears it.
+ * waited_ns (device, int64, 8-byte aligned) receives the time the wait took.
+ * The pages have no counterpart of this call (they ask only that failures be
+ * tested).
+ */
+ra_status ring_attn_wait_selfcheck(int limit_ms, int64_t* waited_ns, void* stream);
+
 /* ring_attn_last_error -- message for the last failing call on this host thread. */
 const char* ring_attn_last_error(void);
 

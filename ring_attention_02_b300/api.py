@@ -58,12 +58,14 @@ def lib() -> ctypes.CDLL:
             L.ring_attn_index_map.argtypes = [i64, i32, i32, vp]
             L.ring_attn_census.argtypes = [i64, i32, i32, i32, vp, vp]
             L.ring_attn_check_status.argtypes = [vp]
+            L.ring_attn_wait_selfcheck.argtypes = [i32, vp, vp]
             L.ring_attn_last_error.restype = ctypes.c_char_p
             L.ring_attn_version.restype = ctypes.c_char_p
             for name in ("ring_attn_fwd", "ring_attn_fwd_counted", "ring_attn_bwd",
                          "ring_attn_bwd_noalloc", "ring_attn_decode",
                          "ring_attn_step", "ring_attn_merge", "ring_attn_permute",
-                         "ring_attn_index_map", "ring_attn_census", "ring_attn_check_status"):
+                         "ring_attn_index_map", "ring_attn_census", "ring_attn_check_status",
+                         "ring_attn_wait_selfcheck"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -250,6 +252,15 @@ def census(S: int, P: int, layout, causal: bool = True):
 def check_status(stream=None):
     """Synchronises the stream and raises if a kernel reported a timeout."""
     _check(lib().ring_attn_check_status(_stream(stream)))
+
+
+def wait_selfcheck(limit_ms: int = 50, stream=None) -> int:
+    """Runs one bounded wait that is never satisfied (limit_ms milliseconds);
+    returns the nanoseconds it waited.  check_status() then raises
+    RingAttnError(RA_ERR_DEVICE_TIMEOUT) once."""
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    _check(lib().ring_attn_wait_selfcheck(int(limit_ms), _ptr(waited), _stream(stream)))
+    return int(waited.item())
 
 
 def version() -> str:

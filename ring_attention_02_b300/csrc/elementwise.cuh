@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include "geometry.cuh"
+#include "sm103_ptx.cuh"
 
 namespace ra {
 
@@ -82,6 +83,21 @@ __global__ void merge_kernel(float* __restrict__ out_acc, float* __restrict__ ls
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- wait self-check
+// One thread waits on an mbarrier that nothing ever arrives on, with the same
+// bounded wait the kernels use but a caller-chosen limit: the wait gives up,
+// records RA_DEV_TIMEOUT_SELFCHECK in the device status word and the kernel
+// returns, leaving the context usable.  *waited_ns receives the time spent.
+__global__ void wait_selfcheck_kernel(unsigned long long limit_ns, unsigned long long* waited_ns) {
+  __shared__ uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  const unsigned long long t0 = globaltimer();
+  const bool ok = mbar_wait_for(b, 0, RA_DEV_TIMEOUT_SELFCHECK, limit_ns);
+  *waited_ns = ok ? 0ull : globaltimer() - t0;
 }
 
 }  // namespace ra

@@ -663,6 +663,21 @@ ra_status ring_attn_check_status(void* stream) {
   return RA_OK;
 }
 
+ra_status ring_attn_wait_selfcheck(int limit_ms, int64_t* waited_ns, void* stream) {
+  if (!waited_ns) return fail(RA_ERR_NULL, "waited_ns must be non-NULL");
+  if (limit_ms < 1 || limit_ms > 1000)
+    return fail(RA_ERR_SHAPE, "limit_ms=%d outside [1, 1000]", limit_ms);
+  if (reinterpret_cast<uintptr_t>(waited_ns) & 7u) return fail(RA_ERR_ALIGN, "waited_ns must be 8-byte aligned");
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  ra::wait_selfcheck_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+      (unsigned long long)limit_ms * 1000000ull, reinterpret_cast<unsigned long long*>(waited_ns));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "wait_selfcheck_kernel launch");
+  return RA_OK;
+}
+
 const char* ring_attn_last_error(void) { return g_last_error; }
 
 const char* ring_attn_version(void) { return "ring_attn 0.1.0 (sm_103a)"; }

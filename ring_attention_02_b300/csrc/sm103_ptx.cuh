@@ -21,6 +21,7 @@ enum : unsigned int {
   RA_DEV_TIMEOUT_MMA = 2u,
   RA_DEV_TIMEOUT_SOFTMAX = 4u,
   RA_DEV_TIMEOUT_DRAIN = 8u,
+  RA_DEV_TIMEOUT_SELFCHECK = 16u,
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -59,6 +60,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// Bounded wait with an explicit limit (used by the wait self-check; the
+// kernels' waits below use kWaitLimitNs).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned int err_code,
+                                              unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > limit_ns) {
+      atomicOr(&g_dev_status, err_code);
+      return false;
+    }
+  }
 }
 
 // Bounded wait for the phase of `parity` to complete.  `abort_flag` (shared
