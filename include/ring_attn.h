@@ -99,6 +99,26 @@ ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out,
                         void* stream);
 
 /*
+ * ring_attn_fwd_varlen -- ring_attn_fwd over packed sequences: nseq sequences
+ * of different lengths laid end to end, each one split over the P ranks by
+ * `layout` on its own and attending only within itself.  This is the next step
+ * the pages point to beyond one sequence: sequence parallelism for long
+ * documents and code bases in training and inference ("Die Zukunft ..." and
+ * its use cases); the packing itself is this library's reading.
+ *   cu_seqlens: HOST array of nseq+1 int64 token offsets, cu_seqlens[0] = 0,
+ *               sequence i holds tokens [cu_seqlens[i], cu_seqlens[i+1]);
+ *               every length must be divisible by P (by 2P for zig-zag).
+ *   q, out [total][H][D]; k, v [total][Hkv][D] (total = cu_seqlens[nseq]);
+ *   lse [H][total] fp32 or NULL.  Other rules as ring_attn_fwd.
+ * The call copies a work list (longest first) and cu_seqlens to the device
+ * with cudaMallocAsync / cudaMemcpyAsync / cudaFreeAsync on `stream`.
+ */
+ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                               ra_dtype out_dtype, float* lse, const int64_t* cu_seqlens, int nseq,
+                               int H, int Hkv, int D, int P, ra_layout layout, int causal,
+                               float scale, void* stream);
+
+/*
  * ring_attn_fwd_counted -- ring_attn_fwd that also adds, for each shard r, the
  * number of (128-query tile, 128-key tile) blocks the kernel actually
  * multiplied into shard_tiles[r] (device, int64[P], caller-zeroed).  The

@@ -44,6 +44,8 @@ def lib() -> ctypes.CDLL:
             vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
             L.ring_attn_fwd.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i64, i32, i32,
                                         i32, i32, f32, vp]
+            L.ring_attn_fwd_varlen.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
+                                               i32, i32, i32, f32, vp]
             L.ring_attn_fwd_counted.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i64, i32,
                                                 i32, i32, i32, f32, vp, vp]
             L.ring_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64,
@@ -61,7 +63,8 @@ def lib() -> ctypes.CDLL:
             L.ring_attn_wait_selfcheck.argtypes = [i32, vp, vp]
             L.ring_attn_last_error.restype = ctypes.c_char_p
             L.ring_attn_version.restype = ctypes.c_char_p
-            for name in ("ring_attn_fwd", "ring_attn_fwd_counted", "ring_attn_bwd",
+            for name in ("ring_attn_fwd", "ring_attn_fwd_varlen", "ring_attn_fwd_counted",
+                         "ring_attn_bwd",
                          "ring_attn_bwd_noalloc", "ring_attn_decode",
                          "ring_attn_step", "ring_attn_merge", "ring_attn_permute",
                          "ring_attn_index_map", "ring_attn_census", "ring_attn_check_status",
@@ -115,6 +118,33 @@ def fwd(q, k, v, P: int, layout, causal: bool = True, scale: float | None = None
     _check(lib().ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), odt, _ptr(lse), B, H, Hkv,
                                S, D, P, _layout(layout), int(bool(causal)), float(scale),
                                _stream(stream)))
+    return out, lse
+
+
+def fwd_varlen(q, k, v, cu_seqlens, P: int, layout, causal: bool = True,
+               scale: float | None = None, out_dtype=torch.bfloat16, out=None, lse=None,
+               want_lse: bool = True, stream=None):
+    """Forward over packed sequences.  q [total,H,D], k/v [total,Hkv,D] bf16;
+    cu_seqlens: host int64 offsets (list or CPU tensor) of nseq+1 entries.
+
+    Returns (out [total,H,D], lse [H,total] fp32 or None).
+    """
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, nm)
+    total, H, D = q.shape
+    Hkv = k.shape[1]
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int64).contiguous().cpu()
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((total, H, D), dtype=out_dtype, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    odt = RA_F32 if out.dtype == torch.float32 else RA_BF16
+    _check(lib().ring_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), odt, _ptr(lse),
+                                      ctypes.c_void_p(cu.data_ptr()), len(cu) - 1, H, Hkv, D, P,
+                                      _layout(layout), int(bool(causal)), float(scale),
+                                      _stream(stream)))
     return out, lse
 
 

@@ -69,6 +69,10 @@ struct FwdParams {
   unsigned long long* shard_tiles;  // may be null: per-shard count of multiplied tile pairs
   int64_t num_items;
   int kv_group;        // (b, kv head) pairs per scheduling group (see unit_head)
+  // packed sequences (attn_fwd_kernel<D, true> only):
+  const int4* units;          // (sequence, shard, segment, pair) per unit, longest first
+  const int64_t* cu_seqlens;  // token offset of each sequence in the pack, and the total
+  int total;                  // tokens in the pack
 };
 
 template <int D>
@@ -102,6 +106,8 @@ struct __align__(1024) FwdSmem {
 // Per-unit schedule facts every role derives identically.
 struct UnitHead {
   int b, h, hkv, shard, seg, pair;
+  int row_base;      // token row of position 0 of this (b or sequence) in q/k/v/out
+  int64_t lse0;      // index of position 0 of this (b or sequence, h) in lse
 };
 
 // Work items are ordered group-major: the (b, kv head) pairs are cut into
@@ -110,7 +116,35 @@ struct UnitHead {
 // side (the G query heads of one kv head adjacent).  With one group this is a
 // global longest-first order; smaller groups keep the key/value tiles the
 // running CTAs share inside L2 when all of them would not fit.
-__device__ __forceinline__ UnitHead unit_head(const FwdParams& p, int64_t item) {
+__device__ __forceinline__ UnitHead unit_head_dense(const FwdParams& p, int64_t item);
+
+// Packed sequences: item = unit * H + h over the host's longest-first unit
+// list; the geometry is the unit's sequence's (B = 1, S = its length).
+template <bool kVarlen>
+__device__ __forceinline__ const Geo& unit_head(const FwdParams& p, int64_t item, UnitHead& u,
+                                                Geo& gv) {
+  if constexpr (kVarlen) {
+    const int H = p.g.H;
+    const int64_t unit = item / H;
+    u.h = (int)(item % H);
+    u.hkv = u.h / (H / p.g.Hkv);
+    u.b = 0;
+    const int4 w = __ldg(p.units + unit);
+    const int64_t t0 = __ldg(p.cu_seqlens + w.x), t1 = __ldg(p.cu_seqlens + w.x + 1);
+    gv = make_geo(1, H, p.g.Hkv, t1 - t0, p.g.P, p.g.layout, p.g.causal);
+    u.shard = w.y;
+    u.seg = w.z;
+    u.pair = w.w;
+    u.row_base = (int)t0;
+    u.lse0 = (int64_t)u.h * p.total + t0;
+    return gv;
+  } else {
+    u = unit_head_dense(p, item);
+    return p.g;
+  }
+}
+
+__device__ __forceinline__ UnitHead unit_head_dense(const FwdParams& p, int64_t item) {
   UnitHead u;
   const Geo& g = p.g;
   const int G = g.H / g.Hkv;
@@ -131,6 +165,8 @@ __device__ __forceinline__ UnitHead unit_head(const FwdParams& p, int64_t item) 
   u.shard = w.shard;
   u.seg = w.seg;
   u.pair = w.pair;
+  u.row_base = u.b * g.S;
+  u.lse0 = ((int64_t)u.b * g.H + u.h) * g.S;
   return u;
 }
 
@@ -145,29 +181,30 @@ struct KIter {
   Seg seg;
 };
 
-__device__ __forceinline__ void kiter_setup(const FwdParams& p, int shard, int qmax, KIter& it) {
+__device__ __forceinline__ void kiter_setup(const Geo& g, const FwdParams& p, int shard, int qmax,
+                                            KIter& it) {
   it.t = 0;
-  it.t_end = p.mode == FWD_MODE_STEP ? 1 : p.g.P;
+  it.t_end = p.mode == FWD_MODE_STEP ? 1 : g.P;
   it.sk = 0;
   it.bt = 0;
   it.qmax = qmax;
   it.shard = shard;
-  it.s = p.mode == FWD_MODE_STEP ? p.step_s : ring_block(p.g, shard, 0);
-  it.seg = segment_of(p.g, it.s, 0);
-  it.nk = visible_tiles(p.g, it.seg, qmax);
+  it.s = p.mode == FWD_MODE_STEP ? p.step_s : ring_block(g, shard, 0);
+  it.seg = segment_of(g, it.s, 0);
+  it.nk = visible_tiles(g, it.seg, qmax);
 }
 
 // Advances to the next key tile; false when the schedule is exhausted.
-__device__ __forceinline__ bool kiter_next(const FwdParams& p, KIter& it) {
+__device__ __forceinline__ bool kiter_next(const Geo& g, KIter& it) {
   while (it.bt >= it.nk) {
     it.bt = 0;
-    if (++it.sk >= p.g.nseg) {
+    if (++it.sk >= g.nseg) {
       it.sk = 0;
       if (++it.t >= it.t_end) return false;
-      it.s = ring_block(p.g, it.shard, it.t);
+      it.s = ring_block(g, it.shard, it.t);
     }
-    it.seg = segment_of(p.g, it.s, it.sk);
-    it.nk = visible_tiles(p.g, it.seg, it.qmax);
+    it.seg = segment_of(g, it.s, it.sk);
+    it.nk = visible_tiles(g, it.seg, it.qmax);
   }
   return true;
 }
@@ -178,29 +215,29 @@ __device__ __forceinline__ int kiter_first_pos(const KIter& it) {
 }
 
 // Is the current key tile visible to a query tile whose last position is qmax?
-__device__ __forceinline__ bool visible_to(const FwdParams& p, const KIter& it, int valid,
-                                           int qmax) {
-  return valid && (!p.g.causal || kiter_first_pos(it) <= qmax);
+__device__ __forceinline__ bool visible_to(const Geo& g, const KIter& it, int valid, int qmax) {
+  return valid && (!g.causal || kiter_first_pos(it) <= qmax);
 }
 
 // TMA coordinates (phase, row) of a tile starting at offset `off` of segment
-// (pos0, local0) of shard `shard`, batch b.
-__device__ __forceinline__ void tile_coords(const FwdParams& p, int shard, int pos0, int local0,
-                                            int off, int b, int& phase, int& row) {
-  const Geo& g = p.g;
+// (pos0, local0) of shard `shard`, for the unit's batch entry or sequence
+// whose position 0 sits at token row row_base (a multiple of P).
+__device__ __forceinline__ void tile_coords(const Geo& g, const FwdParams& p, int shard, int pos0,
+                                            int local0, int off, int row_base, int& phase,
+                                            int& row) {
   if (p.mode == FWD_MODE_STEP) {
     phase = 0;
-    row = b * g.n + local0 + off;
+    row = row_base / g.P + local0 + off;     // shard-local tensors: n rows per batch entry
   } else if (g.layout == LAYOUT_STRIPED) {
     phase = shard;
-    row = b * g.n + off;
+    row = row_base / g.P + off;
   } else {
     phase = 0;
-    row = b * g.S + pos0 + off;
+    row = row_base + pos0 + off;
   }
 }
 
-template <int D>
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -243,7 +280,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const Geo& g = p.g;
   const int sblk = step_block(p);
 
   // Static "snake" assignment of the longest-first item list: round k gives
@@ -267,7 +303,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
-        const UnitHead u = unit_head(p, item);
+        UnitHead u;
+        Geo gv;
+        const Geo& g = unit_head<kVarlen>(p, item, u, gv);
         const QTile qa = make_qtile(g, u.shard, u.seg, 2 * u.pair);
         const QTile qb = make_qtile(g, u.shard, u.seg, 2 * u.pair + 1);
         const int na = tile_work(g, qa, sblk), nb = tile_work(g, qb, sblk);
@@ -282,17 +320,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const uint32_t bar = smem_u32(&sm.q_full[x]);
           mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
           int phase, row;
-          tile_coords(p, qt.shard, qt.pos0, qt.local0, qt.off, u.b, phase, row);
+          tile_coords(g, p, qt.shard, qt.pos0, qt.local0, qt.off, u.row_base, phase, row);
 #pragma unroll
           for (int st = 0; st < Cfg::kSubTiles; ++st)
             tma_load_4d(smem_u32(sm.q[x]) + st * (kTile * 128), &tm_q, bar, 64 * st, u.h, phase,
                         row, pol_q);
         }
         KIter it;
-        kiter_setup(p, u.shard, qb.valid && qb.qmax > qa.qmax ? qb.qmax : qa.qmax, it);
-        while (kiter_next(p, it)) {
+        kiter_setup(g, p, u.shard, qb.valid && qb.qmax > qa.qmax ? qb.qmax : qa.qmax, it);
+        while (kiter_next(g, it)) {
           int phase, row;
-          tile_coords(p, it.s, it.seg.pos0, it.seg.local0, it.bt * kTile, u.b, phase, row);
+          tile_coords(g, p, it.s, it.seg.pos0, it.seg.local0, it.bt * kTile, u.row_base, phase,
+                      row);
           if (!mbar_wait(smem_u32(&sm.k_empty[kst]), k_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
             goto done;
           uint32_t bar = smem_u32(&sm.k_full[kst]);
@@ -330,7 +369,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
-        const UnitHead u = unit_head(p, item);
+        UnitHead u;
+        Geo gv;
+        const Geo& g = unit_head<kVarlen>(p, item, u, gv);
         const QTile qa = make_qtile(g, u.shard, u.seg, 2 * u.pair);
         const QTile qb = make_qtile(g, u.shard, u.seg, 2 * u.pair + 1);
         const int na = tile_work(g, qa, sblk), nb = tile_work(g, qb, sblk);
@@ -343,12 +384,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool pend = false;   // a P V of the previous key tile is owed
         int prev_vst = -1;
         KIter it;
-        kiter_setup(p, u.shard, qb.valid && qb.qmax > qa.qmax ? qb.qmax : qa.qmax, it);
-        bool more = kiter_next(p, it);
+        kiter_setup(g, p, u.shard, qb.valid && qb.qmax > qa.qmax ? qb.qmax : qa.qmax, it);
+        bool more = kiter_next(g, it);
         while (true) {
           bool act = false;
           if (more) {
-            act = visible_to(p, it, qt.valid, qt.qmax);
+            act = visible_to(g, it, qt.valid, qt.qmax);
             if (!mbar_wait(smem_u32(&sm.k_full[kst]), k_ph, RA_DEV_TIMEOUT_MMA, abort_flag))
               goto done;
             tc_fence_after();
@@ -417,7 +458,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (++kst == Cfg::kKStages) { kst = 0; k_ph ^= 1; }
           prev_vst = (int)vst;
           ++it.bt;
-          more = kiter_next(p, it);
+          more = kiter_next(g, it);
         }
       }
     }
@@ -436,7 +477,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     for (int64_t k = 0;; ++k) {
       const int64_t item = item_at(k);
       if (item >= p.num_items) break;
-      const UnitHead u = unit_head(p, item);
+      UnitHead u;
+      Geo gv;
+      const Geo& g = unit_head<kVarlen>(p, item, u, gv);
       const QTile qt = make_qtile(g, u.shard, u.seg, 2 * u.pair + x);
       if (!qt.valid) continue;
       int qmax_u = qt.qmax;
@@ -451,9 +494,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       float l_run = 0.f;         // running normaliser
       if (ntiles > 0) {
         KIter it;
-        kiter_setup(p, u.shard, qmax_u, it);
-        while (kiter_next(p, it)) {
-          if (!visible_to(p, it, 1, qt.qmax)) { ++it.bt; continue; }
+        kiter_setup(g, p, u.shard, qmax_u, it);
+        while (kiter_next(g, it)) {
+          if (!visible_to(g, it, 1, qt.qmax)) { ++it.bt; continue; }
           const int k0 = it.bt * kTile;
           const int kleft = it.seg.len - k0;
           const int kvalid = kleft < kTile ? kleft : kTile;
@@ -608,8 +651,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         orow = ((int64_t)u.b * g.n + j) * g.H + u.h;
         lidx = ((int64_t)u.b * g.H + u.h) * g.n + j;
       } else {
-        orow = ((int64_t)u.b * g.S + qpos) * g.H + u.h;
-        lidx = ((int64_t)u.b * g.H + u.h) * g.S + qpos;
+        orow = ((int64_t)u.row_base + qpos) * g.H + u.h;
+        lidx = u.lse0 + qpos;
       }
 #pragma unroll
       for (int cch = 0; cch < D / 32; ++cch) {

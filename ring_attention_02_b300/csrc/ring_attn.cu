@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -43,6 +44,7 @@ struct DeviceInfo {
   int cc_major = 0;
   int l2_bytes = 0;
   bool fwd_attr_set[2] = {false, false};
+  bool fwd_varlen_attr_set[2] = {false, false};
   bool bwd_attr_set[2] = {false, false};
   bool dec_attr_set[2] = {false, false};
 };
@@ -136,28 +138,29 @@ ra_status check_common(int B, int H, int Hkv, int64_t S, int D, int P, int layou
   return RA_OK;
 }
 
-template <int D>
+template <int D, bool kVarlen>
 ra_status launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const ra::FwdParams& prm, DeviceInfo* dev, cudaStream_t stream) {
   const size_t smem = sizeof(ra::FwdSmem<D>) + 1024;
   const int di = D == 128 ? 1 : 0;
-  if (!dev->fwd_attr_set[di]) {
+  bool& attr_set = kVarlen ? dev->fwd_varlen_attr_set[di] : dev->fwd_attr_set[di];
+  if (!attr_set) {
     // The kernel moves registers between warpgroups (setmaxnreg); that only
     // completes if the launch holds exactly the budget the split assumes.
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, ra::attn_fwd_kernel<D>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, ra::attn_fwd_kernel<D, kVarlen>);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(fwd)");
     if (fa.numRegs != ra::kRegsLaunch)
       return fail(RA_ERR_UNSUPPORTED, "forward kernel built with %d registers/thread, expected %d",
                   fa.numRegs, ra::kRegsLaunch);
-    e = cudaFuncSetAttribute(ra::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+    e = cudaFuncSetAttribute(ra::attn_fwd_kernel<D, kVarlen>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd smem)");
-    dev->fwd_attr_set[di] = true;
+    attr_set = true;
   }
   if (prm.num_items == 0) return RA_OK;
   const int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
-  ra::attn_fwd_kernel<D><<<(unsigned)grid, 384, smem, stream>>>(mq, mk, mv, prm);
+  ra::attn_fwd_kernel<D, kVarlen><<<(unsigned)grid, 384, smem, stream>>>(mq, mk, mv, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel launch");
   return RA_OK;
@@ -227,8 +230,8 @@ ra_status fwd_impl(int mode, const void* q, const void* k, const void* v, void* 
     if (st == RA_OK) st = make_token_map(&mv, v, D, Hkv, 1, (int64_t)B * S);
   }
   if (st != RA_OK) return st;
-  return D == 128 ? launch_fwd_d<128>(mq, mk, mv, prm, dev, stream)
-                  : launch_fwd_d<64>(mq, mk, mv, prm, dev, stream);
+  return D == 128 ? launch_fwd_d<128, false>(mq, mk, mv, prm, dev, stream)
+                  : launch_fwd_d<64, false>(mq, mk, mv, prm, dev, stream);
 }
 
 struct BwdArgs {
@@ -384,6 +387,43 @@ ra_status launch_decode_d(const CUtensorMap& mk, const CUtensorMap& mv, const ra
   return RA_OK;
 }
 
+// ---------------------------------------------------------------- packed sequences
+// Checks cu_seqlens (host) and builds the longest-first unit list of a pack:
+// (sequence, shard, segment, tile pair), ordered by the key tiles the pair
+// multiplies (ties in pack order).
+ra_status varlen_units(const int64_t* cu, int nseq, int H, int Hkv, int P, int layout, int causal,
+                       std::vector<int4>* units) {
+  if (!cu) return fail(RA_ERR_NULL, "cu_seqlens must be non-NULL");
+  if (nseq < 1) return fail(RA_ERR_SHAPE, "nseq=%d must be positive", nseq);
+  if (cu[0] != 0) return fail(RA_ERR_SHAPE, "cu_seqlens[0]=%lld must be 0", (long long)cu[0]);
+  if (cu[nseq] > 0x7fffffffLL)
+    return fail(RA_ERR_SHAPE, "the pack holds %lld tokens; at most 2^31-1", (long long)cu[nseq]);
+  const int64_t unit_mult = layout == RA_LAYOUT_ZIGZAG ? 2 * (int64_t)P : P;
+  std::vector<std::pair<int, int4>> tmp;
+  for (int i = 0; i < nseq; ++i) {
+    const int64_t L = cu[i + 1] - cu[i];
+    if (L < 1) return fail(RA_ERR_SHAPE, "sequence %d has length %lld", i, (long long)L);
+    if (L % unit_mult != 0)
+      return fail(RA_ERR_LAYOUT, "sequence %d: length %lld not divisible by %lld", i,
+                  (long long)L, (long long)unit_mult);
+    const ra::Geo g = ra::make_geo(1, H, Hkv, L, P, layout, causal ? 1 : 0);
+    for (int r = 0; r < P; ++r)
+      for (int sg = 0; sg < g.nseg; ++sg)
+        for (int pr = 0; pr < g.npair; ++pr) {
+          const ra::QTile qa = ra::make_qtile(g, r, sg, 2 * pr), qb = ra::make_qtile(g, r, sg, 2 * pr + 1);
+          const int cost = ra::tile_work(g, qa, -1) + ra::tile_work(g, qb, -1);
+          if (cost > 0) tmp.push_back({cost, make_int4(i, r, sg, pr)});
+        }
+  }
+  std::stable_sort(tmp.begin(), tmp.end(),
+                   [](const std::pair<int, int4>& a, const std::pair<int, int4>& b) {
+                     return a.first > b.first;
+                   });
+  units->clear();
+  for (auto& t : tmp) units->push_back(t.second);
+  return RA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -395,6 +435,73 @@ ra_status ring_attn_fwd(const void* q, const void* k, const void* v, void* out, 
     return fail(RA_ERR_UNSUPPORTED, "out_dtype %d", (int)out_dtype);
   return fwd_impl(ra::FWD_MODE_RING, q, k, v, out, out_dtype == RA_F32, lse, B, H, Hkv, S, D, P,
                   layout, causal, scale, 0, 0, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                               ra_dtype out_dtype, float* lse, const int64_t* cu_seqlens, int nseq,
+                               int H, int Hkv, int D, int P, ra_layout layout, int causal,
+                               float scale, void* stream) {
+  if (!q || !k || !v || !out) return fail(RA_ERR_NULL, "q, k, v and out must be non-NULL");
+  if (out_dtype != RA_BF16 && out_dtype != RA_F32)
+    return fail(RA_ERR_UNSUPPORTED, "out_dtype %d", (int)out_dtype);
+  if (!cu_seqlens || nseq < 1) return fail(RA_ERR_NULL, "cu_seqlens and nseq >= 1 are required");
+  const int64_t total = cu_seqlens[nseq];
+  ra_status st = check_common(1, H, Hkv, total > 0 ? total : 1, D, P, (int)layout, scale);
+  if (st != RA_OK) return st;
+  std::vector<int4> units;
+  st = varlen_units(cu_seqlens, nseq, H, Hkv, P, (int)layout, causal, &units);
+  if (st != RA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(RA_ERR_ALIGN, "q, k, v and out must be 16-byte aligned");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(RA_ERR_ALIGN, "lse must be 4-byte aligned");
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != RA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (units.empty()) return RA_OK;
+  // the unit list and cu_seqlens go to the device with the call
+  const size_t ub = units.size() * sizeof(int4), cb = (size_t)(nseq + 1) * sizeof(int64_t);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, ub + cb, cs);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(RA_ERR_ALLOC, "cudaMallocAsync(%zu bytes) for the unit list: %s", ub + cb,
+                cudaGetErrorString(e));
+  }
+  e = cudaMemcpyAsync(ws, units.data(), ub, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(static_cast<char*>(ws) + ub, cu_seqlens, cb, cudaMemcpyHostToDevice, cs);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(ws, cs);
+    return cuda_fail(e, "copying the unit list");
+  }
+  ra::FwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.g = ra::make_geo(1, H, Hkv, total, P, (int)layout, causal ? 1 : 0);
+  prm.mode = ra::FWD_MODE_RING;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.out = out;
+  prm.out_f32 = out_dtype == RA_F32;
+  prm.lse = lse;
+  prm.num_items = (int64_t)units.size() * H;
+  prm.kv_group = Hkv;
+  prm.units = static_cast<const int4*>(ws);
+  prm.cu_seqlens = reinterpret_cast<const int64_t*>(static_cast<char*>(ws) + ub);
+  prm.total = (int)total;
+  CUtensorMap mq, mk, mv;
+  const bool striped = layout == RA_LAYOUT_STRIPED;
+  const int64_t phases = striped ? P : 1;
+  const int64_t rows = striped ? total / P : total;
+  st = make_token_map(&mq, q, D, H, phases, rows);
+  if (st == RA_OK) st = make_token_map(&mk, k, D, Hkv, phases, rows);
+  if (st == RA_OK) st = make_token_map(&mv, v, D, Hkv, phases, rows);
+  if (st == RA_OK)
+    st = D == 128 ? launch_fwd_d<128, true>(mq, mk, mv, prm, dev, cs)
+                  : launch_fwd_d<64, true>(mq, mk, mv, prm, dev, cs);
+  e = cudaFreeAsync(ws, cs);
+  if (st != RA_OK) return st;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(unit list)");
+  return RA_OK;
 }
 
 ra_status ring_attn_fwd_counted(const void* q, const void* k, const void* v, void* out,
