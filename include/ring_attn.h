@@ -154,6 +154,20 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
                         int causal, float scale, void* stream);
 
 /*
+ * ring_attn_bwd_varlen -- gradients of ring_attn_fwd_varlen (packed
+ * sequences; same cu_seqlens, layouts and shapes):
+ *   q, out, dout, dq [total][H][D]; k, v, dk, dv [total][Hkv][D];
+ *   lse [H][total] fp32 from ring_attn_fwd_varlen (out bf16).
+ * Each sequence's gradients are those of its own attention.  Takes a
+ * transient workspace (vectors and work lists) with cudaMallocAsync /
+ * cudaMemcpyAsync / cudaFreeAsync on `stream`.
+ */
+ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               const int64_t* cu_seqlens, int nseq, int H, int Hkv, int D, int P,
+                               ra_layout layout, int causal, float scale, void* stream);
+
+/*
  * ring_attn_bwd_noalloc -- ring_attn_bwd for callers that cannot allocate GPU
  * memory while they run: a framework that has already reserved the whole
  * device for its own caching allocator (so a driver allocation from inside

@@ -51,6 +51,8 @@ def lib() -> ctypes.CDLL:
             L.ring_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64,
                                         i32, i32, i32, i32, f32, vp]
             L.ring_attn_bwd_noalloc.argtypes = L.ring_attn_bwd.argtypes
+            L.ring_attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                               i32, i32, i32, i32, i32, f32, vp]
             L.ring_attn_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64,
                                            i32, i32, i32, f32, vp]
             L.ring_attn_step.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, i32, i32,
@@ -65,7 +67,7 @@ def lib() -> ctypes.CDLL:
             L.ring_attn_version.restype = ctypes.c_char_p
             for name in ("ring_attn_fwd", "ring_attn_fwd_varlen", "ring_attn_fwd_counted",
                          "ring_attn_bwd",
-                         "ring_attn_bwd_noalloc", "ring_attn_decode",
+                         "ring_attn_bwd_noalloc", "ring_attn_decode", "ring_attn_bwd_varlen",
                          "ring_attn_step", "ring_attn_merge", "ring_attn_permute",
                          "ring_attn_index_map", "ring_attn_census", "ring_attn_check_status",
                          "ring_attn_wait_selfcheck"):
@@ -181,6 +183,23 @@ def bwd(q, k, v, out, lse, dout, P: int, layout, causal: bool = True,
                                _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, P,
                                _layout(layout), int(bool(causal)), float(scale),
                                _stream(stream)))
+    return dq, dk, dv
+
+
+def bwd_varlen(q, k, v, out, lse, dout, cu_seqlens, P: int, layout, causal: bool = True,
+               scale: float | None = None, stream=None):
+    """Gradients of fwd_varlen: (dq [total,H,D], dk, dv [total,Hkv,D]) bf16."""
+    total, H, D = q.shape
+    Hkv = k.shape[1]
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int64).contiguous().cpu()
+    if scale is None:
+        scale = D ** -0.5
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _check(lib().ring_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                      _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                      ctypes.c_void_p(cu.data_ptr()), len(cu) - 1, H, Hkv, D, P,
+                                      _layout(layout), int(bool(causal)), float(scale),
+                                      _stream(stream)))
     return dq, dk, dv
 
 

@@ -57,6 +57,11 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int64_t num_items;
+  // packed sequences (kernels instantiated with kVarlen = true only):
+  const int4* units;          // (sequence, shard, segment, tile) per unit, longest first
+  const int64_t* cu_seqlens;  // token offset of each sequence, and the total
+  const int64_t* vbase;       // first element of each sequence in the tile-order vectors
+  int total;                  // tokens in the pack
 };
 
 // Tile-order vectors: slab (b, h, shard, seg, tile) holds 128 floats, one per
@@ -80,30 +85,41 @@ struct BwdCfg {
 constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 384;
 
 // TMA coordinates (phase, row) of the tile at offset `off` of the segment
-// starting at position pos0 of shard `shard`, batch b (natural-order tensor).
-__device__ __forceinline__ void bwd_coords(const Geo& g, int shard, int pos0, int off, int b,
-                                           int& phase, int& row) {
+// starting at position pos0 of shard `shard`, for the batch entry or sequence
+// whose position 0 sits at token row row_base (a multiple of P).
+__device__ __forceinline__ void bwd_coords(const Geo& g, int shard, int pos0, int off,
+                                           int row_base, int& phase, int& row) {
   if (g.layout == LAYOUT_STRIPED) {
     phase = shard;
-    row = b * g.n + off;
+    row = row_base / g.P + off;
   } else {
     phase = 0;
-    row = b * g.S + pos0 + off;
+    row = row_base + pos0 + off;
   }
 }
 
 // ---------------------------------------------------------------- prep
 // delta = rowsum(dout * out) and -lse * log2(e) for every query row, in tile
 // order.  D/8 lanes share a row (16 bytes of dout and of out each).
-template <int D>
+// Packed sequences (kVarlen): blockIdx.y is the sequence; its elements start
+// at vbase[seq], its tokens at cu_seqlens[seq], lse is [H][total].
+template <int D, bool kVarlen>
 __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ out,
                                 const __nv_bfloat16* __restrict__ dout,
                                 const float* __restrict__ lse, float* __restrict__ nlse2,
-                                float* __restrict__ ndelta, Geo g) {
+                                float* __restrict__ ndelta, Geo g, const int64_t* cu_seqlens,
+                                const int64_t* vbase_arr, int total) {
   constexpr int kLanes = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanes;
   const int lane = threadIdx.x % 32;
   const int sub = lane / kLanes, piece = lane % kLanes;
+  int64_t tok0 = 0, vbase = 0;
+  if constexpr (kVarlen) {
+    const int seq = blockIdx.y;
+    tok0 = cu_seqlens[seq];
+    vbase = vbase_arr[seq];
+    g = make_geo(1, g.H, g.Hkv, cu_seqlens[seq + 1] - tok0, g.P, g.layout, g.causal);
+  }
   const int64_t rows = vec_elems(g);
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
   const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
@@ -124,7 +140,8 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ out,
       if (i < qt.valid) {
         real = true;
         const int64_t pos = qt.pos0 + (int64_t)qt.stride * (qt.off + i);
-        const int64_t off = (((int64_t)b * g.S + pos) * g.H + h) * D + piece * 8;
+        const int64_t tok = kVarlen ? tok0 + pos : (int64_t)b * g.S + pos;
+        const int64_t off = (tok * g.H + h) * D + piece * 8;
         const uint4 a = __ldg(reinterpret_cast<const uint4*>(out + off));
         const uint4 c = __ldg(reinterpret_cast<const uint4*>(dout + off));
         const uint32_t av[4] = {a.x, a.y, a.z, a.w}, cv[4] = {c.x, c.y, c.z, c.w};
@@ -135,14 +152,14 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ out,
           acc = fmaf(fa.x, fc.x, acc);
           acc = fmaf(fa.y, fc.y, acc);
         }
-        lidx = ((int64_t)b * g.H + h) * g.S + pos;
+        lidx = kVarlen ? (int64_t)h * total + tok : ((int64_t)b * g.H + h) * g.S + pos;
       }
     }
 #pragma unroll
     for (int o = kLanes / 2; o > 0; o /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (e < rows && piece == 0) {
-      ndelta[e] = real ? -acc : 0.f;
-      nlse2[e] = real ? -__ldg(lse + lidx) * 1.4426950408889634f : -INFINITY;
+      ndelta[vbase + e] = real ? -acc : 0.f;
+      nlse2[vbase + e] = real ? -__ldg(lse + lidx) * 1.4426950408889634f : -INFINITY;
     }
   }
 }
@@ -153,6 +170,8 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ out,
 // that see the most queries come first.
 struct KUnit {
   int b, hkv, shard, seg, tile;
+  int row_base;     // token row of position 0 of this batch entry or sequence
+  int64_t vbase;    // first element of this batch entry or sequence in the vectors
 };
 
 __device__ __forceinline__ KUnit kunit_of(const Geo& g, int64_t item) {
@@ -182,6 +201,8 @@ __device__ __forceinline__ KUnit kunit_of(const Geo& g, int64_t item) {
 // dQ pass: work item -> (b, h, query tile), decreasing position within (b, h).
 struct QUnit {
   int b, h, shard, seg, tile;
+  int row_base;
+  int64_t vbase;
 };
 
 __device__ __forceinline__ QUnit qunit_of(const Geo& g, int64_t item) {
@@ -206,6 +227,57 @@ __device__ __forceinline__ QUnit qunit_of(const Geo& g, int64_t item) {
     w.seg = 0;
   }
   return w;
+}
+
+// The unit of a work item and the geometry it runs in: the call's geometry,
+// or for packed sequences the unit's sequence's (B = 1, S = its length; items
+// are unit * Hkv + kv head, resp. unit * H + head, over the host's list).
+template <bool kVarlen>
+__device__ __forceinline__ const Geo& kunit_get(const BwdParams& p, int64_t item, KUnit& w,
+                                                Geo& gv) {
+  if constexpr (kVarlen) {
+    const int64_t unit = item / p.g.Hkv;
+    w.hkv = (int)(item % p.g.Hkv);
+    w.b = 0;
+    const int4 u4 = __ldg(p.units + unit);
+    const int64_t t0 = __ldg(p.cu_seqlens + u4.x), t1 = __ldg(p.cu_seqlens + u4.x + 1);
+    gv = make_geo(1, p.g.H, p.g.Hkv, t1 - t0, p.g.P, p.g.layout, p.g.causal);
+    w.shard = u4.y;
+    w.seg = u4.z;
+    w.tile = u4.w;
+    w.row_base = (int)t0;
+    w.vbase = __ldg(p.vbase + u4.x);
+    return gv;
+  } else {
+    w = kunit_of(p.g, item);
+    w.row_base = w.b * p.g.S;
+    w.vbase = 0;
+    return p.g;
+  }
+}
+
+template <bool kVarlen>
+__device__ __forceinline__ const Geo& qunit_get(const BwdParams& p, int64_t item, QUnit& w,
+                                                Geo& gv) {
+  if constexpr (kVarlen) {
+    const int64_t unit = item / p.g.H;
+    w.h = (int)(item % p.g.H);
+    w.b = 0;
+    const int4 u4 = __ldg(p.units + unit);
+    const int64_t t0 = __ldg(p.cu_seqlens + u4.x), t1 = __ldg(p.cu_seqlens + u4.x + 1);
+    gv = make_geo(1, p.g.H, p.g.Hkv, t1 - t0, p.g.P, p.g.layout, p.g.causal);
+    w.shard = u4.y;
+    w.seg = u4.z;
+    w.tile = u4.w;
+    w.row_base = (int)t0;
+    w.vbase = __ldg(p.vbase + u4.x);
+    return gv;
+  } else {
+    w = qunit_of(p.g, item);
+    w.row_base = w.b * p.g.S;
+    w.vbase = 0;
+    return p.g;
+  }
 }
 
 // Query tiles a key tile meets, in ring order: for each query head of the
@@ -430,7 +502,7 @@ __device__ __forceinline__ void dq_half(uint32_t t_s, uint32_t t_dp, float2 sl2,
 }
 
 // ---------------------------------------------------------------- dK / dV pass
-template <int D>
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -443,7 +515,6 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   const int tid = threadIdx.x;
   const int warp = tid / 32, lane = tid % 32;
   volatile int* abort_flag = &sm.abort_flag;
-  const Geo& g = p.g;
 
   if (tid == 0) {
     mbar_init(smem_u32(&sm.kv_full), 1);
@@ -489,7 +560,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
-        const KUnit w = kunit_of(g, item);
+        KUnit w;
+        Geo gv;
+        const Geo& g = kunit_get<kVarlen>(p, item, w, gv);
         const QTile kt = make_qtile(g, w.shard, w.seg, w.tile);
         QIter it;
         qiter_setup(g, it, w.hkv, w.shard, kt.qmin);
@@ -500,7 +573,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           const uint32_t bar = smem_u32(&sm.kv_full);
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
           int phase, row;
-          bwd_coords(g, w.shard, kt.pos0, kt.off, w.b, phase, row);
+          bwd_coords(g, w.shard, kt.pos0, kt.off, w.row_base, phase, row);
 #pragma unroll
           for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
             tma_load_4d(smem_u32(sm.k) + s2 * (kTile * 128), &tm_k, bar, 64 * s2, w.hkv, phase,
@@ -515,7 +588,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           const uint32_t bar = smem_u32(&sm.st_full[st]);
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes + 2 * Cfg::kVecBytes);
           int phase, row;
-          bwd_coords(g, it.r, it.seg.pos0, it.a * kTile, w.b, phase, row);
+          bwd_coords(g, it.r, it.seg.pos0, it.a * kTile, w.row_base, phase, row);
 #pragma unroll
           for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
             tma_load_4d(smem_u32(sm.q[st]) + s2 * (kTile * 128), &tm_q, bar, 64 * s2, it.h, phase,
@@ -523,7 +596,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tma_load_4d(smem_u32(sm.dO[st]) + s2 * (kTile * 128), &tm_do, bar, 64 * s2, it.h,
                         phase, row, pol_q);
           }
-          const int64_t vt = vec_tile(g, w.b, it.h, it.r, it.sq, it.a) * kTile;
+          const int64_t vt = w.vbase + vec_tile(g, w.b, it.h, it.r, it.sq, it.a) * kTile;
           bulk_load(smem_u32(sm.nlse2[st]), p.nlse2 + vt, Cfg::kVecBytes, bar, pol_q);
           bulk_load(smem_u32(sm.ndelta[st]), p.ndelta + vt, Cfg::kVecBytes, bar, pol_q);
           if (++st == kSt) { st = 0; st_ph ^= 1; }
@@ -546,7 +619,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
-        const KUnit u = kunit_of(g, item);
+        KUnit u;
+        Geo gv;
+        const Geo& g = kunit_get<kVarlen>(p, item, u, gv);
         const QTile kt = make_qtile(g, u.shard, u.seg, u.tile);
         QIter it;
         qiter_setup(g, it, u.hkv, u.shard, kt.qmin);
@@ -618,7 +693,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     for (int64_t k = 0;; ++k) {
       const int64_t item = item_at(k);
       if (item >= p.num_items) break;
-      const KUnit w = kunit_of(g, item);
+      KUnit w;
+      Geo gv;
+      const Geo& g = kunit_get<kVarlen>(p, item, w, gv);
       const QTile kt = make_qtile(g, w.shard, w.seg, w.tile);
       QIter it;
       qiter_setup(g, it, w.hkv, w.shard, kt.qmin);
@@ -664,7 +741,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         __nv_bfloat16* dst = x == 0 ? p.dv : p.dk;
         const float mul = x == 0 ? 1.f : p.scale;
         const uint32_t t_acc = tmem + lane_addr + (x == 0 ? kColAcc0 : kColAcc1);
-        const int64_t orow = ((int64_t)w.b * g.S + kpos) * g.Hkv + w.hkv;
+        const int64_t orow = ((int64_t)w.row_base + kpos) * g.Hkv + w.hkv;
 #pragma unroll
         for (int cch = 0; cch < D / 32; ++cch) {
           uint32_t r[32];
@@ -697,7 +774,7 @@ done:
 }
 
 // ---------------------------------------------------------------- dQ pass
-template <int D>
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -710,7 +787,6 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   const int tid = threadIdx.x;
   const int warp = tid / 32, lane = tid % 32;
   volatile int* abort_flag = &sm.abort_flag;
-  const Geo& g = p.g;
 
   if (tid == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
@@ -756,7 +832,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
-        const QUnit w = qunit_of(g, item);
+        QUnit w;
+        Geo gv;
+        const Geo& g = qunit_get<kVarlen>(p, item, w, gv);
         const QTile qt = make_qtile(g, w.shard, w.seg, w.tile);
         if (!qt.valid) continue;
         KIterB it;
@@ -768,7 +846,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           const uint32_t bar = smem_u32(&sm.q_full);
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
           int phase, row;
-          bwd_coords(g, w.shard, qt.pos0, qt.off, w.b, phase, row);
+          bwd_coords(g, w.shard, qt.pos0, qt.off, w.row_base, phase, row);
 #pragma unroll
           for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
             tma_load_4d(smem_u32(sm.q) + s2 * (kTile * 128), &tm_q, bar, 64 * s2, w.h, phase, row,
@@ -784,7 +862,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           const uint32_t bar = smem_u32(&sm.st_full[st]);
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
           int phase, row;
-          bwd_coords(g, it.s, it.seg.pos0, it.bt * kTile, w.b, phase, row);
+          bwd_coords(g, it.s, it.seg.pos0, it.bt * kTile, w.row_base, phase, row);
 #pragma unroll
           for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
             tma_load_4d(smem_u32(sm.k[st]) + s2 * (kTile * 128), &tm_k, bar, 64 * s2, hkv, phase,
@@ -811,7 +889,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
-        const QUnit u = qunit_of(g, item);
+        QUnit u;
+        Geo gv;
+        const Geo& g = qunit_get<kVarlen>(p, item, u, gv);
         const QTile qt = make_qtile(g, u.shard, u.seg, u.tile);
         if (!qt.valid) continue;
         KIterB it;
@@ -885,14 +965,16 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     for (int64_t k = 0;; ++k) {
       const int64_t item = item_at(k);
       if (item >= p.num_items) break;
-      const QUnit w = qunit_of(g, item);
+      QUnit w;
+      Geo gv;
+      const Geo& g = qunit_get<kVarlen>(p, item, w, gv);
       const QTile qt = make_qtile(g, w.shard, w.seg, w.tile);
       if (!qt.valid) continue;
       KIterB it;
       kiterb_setup(g, it, w.shard, qt.qmax);
       if (!kiterb_next(g, it)) continue;
       const int qpos = qt.pos0 + qt.stride * (qt.off + row);
-      const int64_t vi = vec_tile(g, w.b, w.h, w.shard, w.seg, w.tile) * kTile + row;
+      const int64_t vi = w.vbase + vec_tile(g, w.b, w.h, w.shard, w.seg, w.tile) * kTile + row;
       const float nl = __ldg(p.nlse2 + vi);
       const float nd = __ldg(p.ndelta + vi);
       const float2 sl2_2 = make_float2(sl2, sl2), nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
@@ -928,7 +1010,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tc_fence_after();
       {
         const uint32_t t_acc = tmem + lane_addr + kColAcc0 + x * (D / 2);
-        const int64_t orow = ((int64_t)w.b * g.S + qpos) * g.H + w.h;
+        const int64_t orow = ((int64_t)w.row_base + qpos) * g.H + w.h;
 #pragma unroll
         for (int cch = 0; cch < D / 64; ++cch) {
           uint32_t r[32];

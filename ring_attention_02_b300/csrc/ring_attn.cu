@@ -45,7 +45,7 @@ struct DeviceInfo {
   int l2_bytes = 0;
   bool fwd_attr_set[2] = {false, false};
   bool fwd_varlen_attr_set[2] = {false, false};
-  bool bwd_attr_set[2] = {false, false};
+  bool bwd_attr_set[4] = {false, false, false, false};
   bool dec_attr_set[2] = {false, false};
 };
 std::mutex g_dev_mu;
@@ -257,20 +257,31 @@ ra_status check_bwd(const BwdArgs& a) {
   return RA_OK;
 }
 
+template <int D, bool kVarlen>
+ra_status bwd_attrs(DeviceInfo* dev) {
+  const size_t smem_kv = sizeof(ra::DkdvSmem<D>) + 1024;
+  const size_t smem_q = sizeof(ra::DqSmem<D>) + 1024;
+  const int di = (D == 128 ? 1 : 0) + (kVarlen ? 2 : 0);
+  if (!dev->bwd_attr_set[di]) {
+    cudaError_t e = cudaFuncSetAttribute(ra::attn_bwd_dkdv_kernel<D, kVarlen>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dkdv smem)");
+    e = cudaFuncSetAttribute(ra::attn_bwd_dq_kernel<D, kVarlen>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_q);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dq smem)");
+    dev->bwd_attr_set[di] = true;
+  }
+  return RA_OK;
+}
+
 template <int D>
 ra_status launch_bwd_d(const BwdArgs& a, float* nlse2, float* ndelta, DeviceInfo* dev,
                        cudaStream_t stream) {
   const size_t smem_kv = sizeof(ra::DkdvSmem<D>) + 1024;
   const size_t smem_q = sizeof(ra::DqSmem<D>) + 1024;
-  const int di = D == 128 ? 1 : 0;
-  if (!dev->bwd_attr_set[di]) {
-    cudaError_t e = cudaFuncSetAttribute(ra::attn_bwd_dkdv_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dkdv smem)");
-    e = cudaFuncSetAttribute(ra::attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_q);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dq smem)");
-    dev->bwd_attr_set[di] = true;
+  {
+    ra_status st0 = bwd_attrs<D, false>(dev);
+    if (st0 != RA_OK) return st0;
   }
   ra::BwdParams prm;
   memset(&prm, 0, sizeof(prm));
@@ -301,22 +312,22 @@ ra_status launch_bwd_d(const BwdArgs& a, float* nlse2, float* ndelta, DeviceInfo
   int64_t blocks = (vrows + rows_per_block - 1) / rows_per_block;
   const int64_t cap = (int64_t)dev->sms * 8;
   if (blocks > cap) blocks = cap;
-  ra::bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
+  ra::bwd_prep_kernel<D, false><<<(unsigned)blocks, 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
-      nlse2, ndelta, g);
+      nlse2, ndelta, g, nullptr, nullptr, 0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bwd_prep_kernel launch");
 
   const int64_t units = (int64_t)g.P * g.nseg * g.ntile;
   prm.num_items = units * a.B * a.Hkv;
   int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
-  ra::attn_bwd_dkdv_kernel<D><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
+  ra::attn_bwd_dkdv_kernel<D, false><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dkdv_kernel launch");
 
   prm.num_items = units * a.B * a.H;
   grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
-  ra::attn_bwd_dq_kernel<D><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
+  ra::attn_bwd_dq_kernel<D, false><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dq_kernel launch");
   return RA_OK;
@@ -421,6 +432,40 @@ ra_status varlen_units(const int64_t* cu, int nseq, int H, int Hkv, int P, int l
                    });
   units->clear();
   for (auto& t : tmp) units->push_back(t.second);
+  return RA_OK;
+}
+
+// Backward over packed sequences: unit lists, vector offsets and the launches.
+template <int D>
+ra_status launch_bwd_varlen_d(const BwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                              const CUtensorMap& mv, const CUtensorMap& mdo, ra::BwdParams prm,
+                              int nseq, int64_t max_vec, int nk, int nq, DeviceInfo* dev,
+                              cudaStream_t stream) {
+  ra_status st = bwd_attrs<D, true>(dev);
+  if (st != RA_OK) return st;
+  const size_t smem_kv = sizeof(ra::DkdvSmem<D>) + 1024;
+  const size_t smem_q = sizeof(ra::DqSmem<D>) + 1024;
+  const int rows_per_block = 8 * (32 / (D / 8));
+  int64_t bx = (max_vec + rows_per_block - 1) / rows_per_block;
+  if (bx > (int64_t)dev->sms * 8) bx = (int64_t)dev->sms * 8;
+  ra::bwd_prep_kernel<D, true><<<dim3((unsigned)bx, (unsigned)nseq), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
+      const_cast<float*>(prm.nlse2), const_cast<float*>(prm.ndelta), prm.g, prm.cu_seqlens,
+      prm.vbase, prm.total);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bwd_prep_kernel launch");
+  const int4* qunits = prm.units + nk;
+  prm.num_items = (int64_t)nk * a.Hkv;
+  int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  ra::attn_bwd_dkdv_kernel<D, true><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dkdv_kernel launch");
+  prm.units = qunits;
+  prm.num_items = (int64_t)nq * a.H;
+  grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  ra::attn_bwd_dq_kernel<D, true><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dq_kernel launch");
   return RA_OK;
 }
 
@@ -542,6 +587,107 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
   float* nlse2 = static_cast<float*>(ws);
   float* ndelta = reinterpret_cast<float*>(static_cast<char*>(ws) + vec_bytes);
   st = bwd_launch(a, nlse2, ndelta, cs);
+  e = cudaFreeAsync(ws, cs);
+  if (st != RA_OK) return st;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(backward workspace)");
+  return RA_OK;
+}
+
+ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* out,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               const int64_t* cu_seqlens, int nseq, int H, int Hkv, int D, int P,
+                               ra_layout layout, int causal, float scale, void* stream) {
+  if (!cu_seqlens || nseq < 1) return fail(RA_ERR_NULL, "cu_seqlens and nseq >= 1 are required");
+  const int64_t total = cu_seqlens[nseq];
+  BwdArgs a{q, k, v, out, lse, dout, dq, dk, dv, 1, H, Hkv, total > 0 ? total : 1, D, P,
+            (int)layout, causal, scale};
+  ra_status st = check_bwd(a);
+  if (st != RA_OK) return st;
+  std::vector<int4> fwd_units;   // validates cu_seqlens against the layout
+  st = varlen_units(cu_seqlens, nseq, H, Hkv, P, (int)layout, causal, &fwd_units);
+  if (st != RA_OK) return st;
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != RA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // key-tile and query-tile units, longest first; vector offsets per sequence
+  std::vector<std::pair<int64_t, int4>> ku, qu;
+  std::vector<int64_t> vbase(nseq);
+  int64_t V = 0, max_vec = 0;
+  for (int i = 0; i < nseq; ++i) {
+    const ra::Geo g = ra::make_geo(1, H, Hkv, cu_seqlens[i + 1] - cu_seqlens[i], P, (int)layout,
+                                   causal ? 1 : 0);
+    vbase[i] = V;
+    V += ra::vec_elems(g);
+    if (ra::vec_elems(g) > max_vec) max_vec = ra::vec_elems(g);
+    for (int r = 0; r < P; ++r)
+      for (int sg = 0; sg < g.nseg; ++sg)
+        for (int t = 0; t < g.ntile; ++t) {
+          const ra::QTile tl = ra::make_qtile(g, r, sg, t);
+          if (!tl.valid) continue;
+          qu.push_back({ra::tile_work(g, tl, -1), make_int4(i, r, sg, t)});
+          int64_t cost = 0;   // query tiles this key tile meets
+          for (int rq = 0; rq < P; ++rq)
+            for (int sq = 0; sq < g.nseg; ++sq) {
+              const ra::Seg qs = ra::segment_of(g, rq, sq);
+              const int first = g.causal ? ra::count_le(qs, tl.qmin - 1) : 0;
+              if (first < qs.len) cost += g.ntile - first / ra::kTile;
+            }
+          ku.push_back({cost, make_int4(i, r, sg, t)});
+        }
+  }
+  auto by_cost = [](const std::pair<int64_t, int4>& x, const std::pair<int64_t, int4>& y) {
+    return x.first > y.first;
+  };
+  std::stable_sort(ku.begin(), ku.end(), by_cost);
+  std::stable_sort(qu.begin(), qu.end(), by_cost);
+  std::vector<int4> units;
+  for (auto& x : ku) units.push_back(x.second);
+  for (auto& x : qu) units.push_back(x.second);
+  const int nk = (int)ku.size(), nq = (int)qu.size();
+  // workspace: nlse2, ndelta [V] fp32 | units | cu_seqlens | vbase
+  const size_t vb = (size_t)V * sizeof(float), ub = units.size() * sizeof(int4);
+  const size_t cb = (size_t)(nseq + 1) * sizeof(int64_t), bb = (size_t)nseq * sizeof(int64_t);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, 2 * vb + ub + cb + bb, cs);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(RA_ERR_ALLOC, "cudaMallocAsync(%zu bytes) for the backward workspace: %s",
+                2 * vb + ub + cb + bb, cudaGetErrorString(e));
+  }
+  char* w8 = static_cast<char*>(ws);
+  e = cudaMemcpyAsync(w8 + 2 * vb, units.data(), ub, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(w8 + 2 * vb + ub, cu_seqlens, cb, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(w8 + 2 * vb + ub + cb, vbase.data(), bb, cudaMemcpyHostToDevice, cs);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(ws, cs);
+    return cuda_fail(e, "copying the unit lists");
+  }
+  ra::BwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.g = ra::make_geo(1, H, Hkv, total, P, (int)layout, causal ? 1 : 0);
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.nlse2 = reinterpret_cast<float*>(w8);
+  prm.ndelta = reinterpret_cast<float*>(w8 + vb);
+  prm.dq = static_cast<__nv_bfloat16*>(dq);
+  prm.dk = static_cast<__nv_bfloat16*>(dk);
+  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.units = reinterpret_cast<const int4*>(w8 + 2 * vb);
+  prm.cu_seqlens = reinterpret_cast<const int64_t*>(w8 + 2 * vb + ub);
+  prm.vbase = reinterpret_cast<const int64_t*>(w8 + 2 * vb + ub + cb);
+  prm.total = (int)total;
+  CUtensorMap mq, mk, mv, mdo;
+  const bool striped = layout == RA_LAYOUT_STRIPED;
+  const int64_t phases = striped ? P : 1;
+  const int64_t rows = striped ? total / P : total;
+  st = make_token_map(&mq, q, D, H, phases, rows);
+  if (st == RA_OK) st = make_token_map(&mk, k, D, Hkv, phases, rows);
+  if (st == RA_OK) st = make_token_map(&mv, v, D, Hkv, phases, rows);
+  if (st == RA_OK) st = make_token_map(&mdo, dout, D, H, phases, rows);
+  if (st == RA_OK)
+    st = D == 128 ? launch_bwd_varlen_d<128>(a, mq, mk, mv, mdo, prm, nseq, max_vec, nk, nq, dev, cs)
+                  : launch_bwd_varlen_d<64>(a, mq, mk, mv, mdo, prm, nseq, max_vec, nk, nq, dev, cs);
   e = cudaFreeAsync(ws, cs);
   if (st != RA_OK) return st;
   if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(backward workspace)");
