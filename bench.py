@@ -15,7 +15,8 @@ dO), counted as 3.5x the forward's flops.
 per-hop form of the whole ring: P*P ``ring_attn_step`` calls and the
 ``ring_attn_merge`` folds, on shard-major inputs permuted beforehand) or
 ``decode`` (``--decode-tokens`` new tokens against the workload's key/value
-cache, HBM bound).
+cache, HBM bound) or ``varlen`` (the forward over a pack of 16 documents with
+a seeded log-uniform length mix of 2k..32k tokens, on the workload's heads).
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle instead
 (bounded samples of the same workload on the host cores).
@@ -38,7 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from ring_attention_02_b300.inputs import (HEADLINE, Workload, by_name, make_dout,  # noqa: E402
-                                           make_for)
+                                           make_for, make_qkv)
 
 METRIC = "causal ring-attn fwd TFLOP/s (bf16, S=128k, 1 B300) and % of BF16 tensor peak"
 METRIC_TRAIN = "causal ring-attn fwd+bwd TFLOP/s (bf16, 1 B300; bwd counted as 2.5x fwd)"
@@ -478,6 +479,26 @@ def run_op(args, w: Workload, rank: int, world: int):
         metric = f"ring_attn_decode HBM GB/s ({T} new token(s) against the sharded cache)"
         dtype = "bf16"
         launches_per_step = 2
+    elif args.op == "varlen":
+        # a pack of documents with a seeded length mix, on the workload's heads,
+        # head dim, ranks and layout; counted flops per sequence
+        from ring_attention_02_b300.inputs import pack_lengths
+        mult = 2 * w.P * 128 if w.layout == "zigzag" else w.P * 128
+        lengths = pack_lengths(16, 2048, 32768, mult, seed=args.seed)
+        total = sum(lengths)
+        cu = torch.tensor([0] + np.cumsum(lengths).tolist(), dtype=torch.int64)
+        qv, kv_, vv = (t[0] for t in make_qkv(1, w.H, w.Hkv, total, w.D, seed=args.seed,
+                                              device=dev))
+        out_v = torch.empty_like(qv)
+        lse_v = torch.empty((w.H, total), dtype=torch.float32, device=dev)
+        step = lambda: api.fwd_varlen(qv, kv_, vv, cu, w.P, w.layout, w.causal, out=out_v,
+                                      lse=lse_v, stream=stream)
+        work = sum(4.0 * w.H * L * L * w.D / (2 if w.causal else 1) for L in lengths)
+        unit, bound = UNIT, "tensor"
+        peak, _, peak_src = measured_peaks()
+        metric = (f"causal ring-attn fwd over a pack of 16 documents TFLOP/s "
+                  f"({total} tokens, lengths {min(lengths)}..{max(lengths)})")
+        dtype = "bf16"
     else:
         qs = api.permute(q, w.S, w.P, w.layout).view(w.B, w.P, n, w.H, w.D)
         ks = api.permute(k, w.S, w.P, w.layout).view(w.B, w.P, n, w.Hkv, w.D)
@@ -557,7 +578,7 @@ def main(argv=None):
                     help="training workloads: tokens of the oracle's fwd+bwd sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-tokens", type=int, default=1, help="--op decode: new tokens T")
-    ap.add_argument("--op", choices=["fwd", "permute", "merge", "step_merge", "decode"],
+    ap.add_argument("--op", choices=["fwd", "permute", "merge", "step_merge", "decode", "varlen"],
                     default="fwd",
                     help="fwd: the workload's step (default); the others time one call")
     args = ap.parse_args(argv)

@@ -102,3 +102,16 @@ def make_dout(B, H, S, D, seed: int = 0, device="cpu") -> torch.Tensor:
 
 def make_for(w: Workload, seed: int = 0, device="cpu"):
     return make_qkv(w.B, w.H, w.Hkv, w.S, w.D, seed=seed, device=device)
+
+
+def pack_lengths(count: int, lo: int, hi: int, multiple: int, seed: int = 0):
+    """Seeded document lengths for a packed batch: log-uniform in [lo, hi],
+    rounded down to a multiple of `multiple` (so every sequence splits evenly
+    over the ranks), at least `multiple`."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 4)
+    u = torch.rand(count, generator=g, dtype=torch.float64)
+    L = torch.exp(torch.log(torch.tensor(float(lo))) + u * (torch.log(torch.tensor(float(hi)))
+                                                          - torch.log(torch.tensor(float(lo)))))
+    return [max(multiple, int(x) // multiple * multiple) for x in L.tolist()]
+
