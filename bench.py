@@ -281,36 +281,63 @@ def run_reference(args, w: Workload, rank: int):
     print(json.dumps(line), flush=True)
 
 
-def measure_e2e(w, api, step_fn, dev_in, dev_out, stream, dev, flops, world, steps):
-    """Same metric through the public calls with host buffers: each step copies
-    its inputs from pinned host memory, runs the step and copies its results
-    back to pinned host memory, all inside the timed region."""
+def measure_e2e(w, api, make_step, dev_in, dev_out, dev_scratch, dev, flops, world, steps):
+    """Same metric through the public calls with host buffers: every step
+    copies its inputs from pinned host memory to the device, runs the step and
+    copies its results back to pinned host memory, all inside the timed region.
+    Steps are pipelined the way a serving or training loop runs them: two
+    device buffer sets, and separate streams for host-to-device copies, compute
+    and device-to-host copies, so step i's copies overlap step i-1's compute.
+    make_step(ins, outs, scratch, stream) runs one step on one buffer set."""
     host_in = [t.cpu().pin_memory() for t in dev_in]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out]
+    sets = [(dev_in, dev_out, dev_scratch),
+            ([torch.empty_like(t) for t in dev_in], [torch.empty_like(t) for t in dev_out],
+             [torch.empty_like(t) for t in dev_scratch])]
+    s_h2d, s_cmp, s_d2h = (torch.cuda.Stream(dev) for _ in range(3))
 
-    def e2e_step():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        step_fn()
-        for h, d in zip(host_out, dev_out):
-            h.copy_(d, non_blocking=True)
+    def run(n, start_evt=None, end_evt=None):
+        ev = lambda: torch.cuda.Event()
+        in_ready, comp_done, out_done = [ev() for _ in range(n)], [ev() for _ in range(n)], \
+            [ev() for _ in range(n)]
+        if start_evt is not None:
+            start_evt.record(s_h2d)
+        for i in range(n):
+            ins, outs, scratch = sets[i % 2]
+            with torch.cuda.stream(s_h2d):
+                if i >= 2:
+                    s_h2d.wait_event(comp_done[i - 2])      # this set's inputs are free again
+                for d, h in zip(ins, host_in):
+                    d.copy_(h, non_blocking=True)
+                in_ready[i].record(s_h2d)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(in_ready[i])
+                if i >= 2:
+                    s_cmp.wait_event(out_done[i - 2])       # this set's results were copied out
+                make_step(ins, outs, scratch, s_cmp)
+                comp_done[i].record(s_cmp)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(comp_done[i])
+                for h, d in zip(host_out, outs):
+                    h.copy_(d, non_blocking=True)
+                out_done[i].record(s_d2h)
+        if end_evt is not None:
+            end_evt.record(s_d2h)
 
-    e2e_step()
+    run(2)
     torch.cuda.synchronize(dev)
-    n = max(1, min(steps, 3))
+    n = max(2, steps)
     _barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n):
-        e2e_step()
-    e1.record(stream)
+    run(n, e0, e1)
     torch.cuda.synchronize(dev)
-    api.check_status(stream)
+    api.check_status(s_cmp)
     ms = max_over_ranks(e0.elapsed_time(e1)) / n
     h2d = sum(t.numel() * t.element_size() for t in dev_in)
     d2h = sum(t.numel() * t.element_size() for t in dev_out)
     return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
+            "pipelined": "double-buffered; H2D, compute and D2H on separate streams"}
 
 
 def run_ours(args, w: Workload, rank: int, world: int):
@@ -370,10 +397,18 @@ def run_ours(args, w: Workload, rank: int, world: int):
     e2e = None
     if not args.skip_e2e:
         if w.backward:
-            e2e = measure_e2e(w, api, step, [q, k, v, do], [dq, dk, dv], stream, dev, flops,
-                              world, args.steps)
+            def make_step(ins, outs, scratch, st):
+                o, l = scratch
+                api.fwd(ins[0], ins[1], ins[2], w.P, w.layout, w.causal, out=o, lse=l, stream=st)
+                api.bwd(ins[0], ins[1], ins[2], o, l, ins[3], w.P, w.layout, w.causal,
+                        dq=outs[0], dk=outs[1], dv=outs[2], stream=st)
+            e2e = measure_e2e(w, api, make_step, [q, k, v, do], [dq, dk, dv], [out, lse], dev,
+                              flops, world, args.steps)
         else:
-            e2e = measure_e2e(w, api, step, [q, k, v], [out, lse], stream, dev, flops, world,
+            def make_step(ins, outs, scratch, st):
+                api.fwd(ins[0], ins[1], ins[2], w.P, w.layout, w.causal, out=outs[0],
+                        lse=outs[1], stream=st)
+            e2e = measure_e2e(w, api, make_step, [q, k, v], [out, lse], [], dev, flops, world,
                               args.steps)
     if rank != 0:
         return
