@@ -171,6 +171,40 @@ def test_ring_of_steps_and_merges_equals_fused(layout):
         assert max_abs(to64(acc_l), rl[:, :, pos[r]]) <= LSE_TOL
 
 
+def test_ring_of_steps_and_merges_at_the_headline_shapes():
+    # the per-hop form on the 128k GQA zig-zag shapes: P*P steps and the merges
+    # of every shard, sampled rows against the oracle
+    w = GQA_128K.with_layout("zigzag")
+    q, k, v = make_qkv(w.B, w.H, w.Hkv, w.S, w.D, seed=7, device="cuda")
+    n = w.S // w.P
+    qs = api.permute(q, w.S, w.P, w.layout).view(w.B, w.P, n, w.H, w.D)
+    ks = api.permute(k, w.S, w.P, w.layout).view(w.B, w.P, n, w.Hkv, w.D)
+    vs = api.permute(v, w.S, w.P, w.layout).view(w.B, w.P, n, w.Hkv, w.D)
+    pos = oracle.layout_positions(w.S, w.P, w.layout)
+    rng = np.random.default_rng(7)
+    eo = el = 0.0
+    for r in range(w.P):
+        qr = qs[:, r].contiguous()
+        acc_o, acc_l = api.step(qr, ks[:, r].contiguous(), vs[:, r].contiguous(), w.S, w.P,
+                                w.layout, r, r, True)
+        for t in range(1, w.P):
+            s_ = (r - t) % w.P
+            po, pl = api.step(qr, ks[:, s_].contiguous(), vs[:, s_].contiguous(), w.S, w.P,
+                              w.layout, r, s_, True)
+            api.merge(acc_o, acc_l, po, pl)
+        api.check_status()
+        slots = np.unique(np.concatenate([[0, n - 1, n // 2 - 1, n // 2],
+                                          rng.integers(0, n, size=6)]))
+        rows = pos[r][slots]
+        ro, rl = oracle.attn_fwd_rows(to64(q[:, torch.from_numpy(rows).cuda()]), rows, to64(k),
+                                      to64(v), True, w.scale)
+        sl = torch.from_numpy(slots).cuda()
+        eo = max(eo, max_abs(to64(acc_o[:, sl]), ro))
+        el = max(el, max_abs(to64(acc_l[:, :, sl]), rl))
+    print(f"PARITY step+merge ring {w.name}: max|out|={eo:.3e} max|lse|={el:.3e}")
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_merge_matches_oracle_with_empty_rows(D):
     B, n, H = 2, 300, 3
