@@ -36,51 +36,65 @@ __global__ void permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restr
 // (out_acc, lse_acc) <- fold of (out_part, lse_part), rows (b, j, h):
 //   lse = max + ln(e^(l1 - max) + e^(l2 - max)),
 //   out = e^(l1 - lse) out_acc + e^(l2 - lse) out_part.
-// One row is handled by D/4 consecutive lanes of one warp (float4 each); the
-// row's lse is read by all of them before lane 0 of the row writes it back.
-template <int D>
-__global__ void merge_kernel(float* __restrict__ out_acc, float* __restrict__ lse_acc,
-                             const float* __restrict__ out_part,
-                             const float* __restrict__ lse_part, int B, int H, int64_t n) {
+// One row is handled by D/4 consecutive lanes of one warp (float4 each).  A
+// warp takes kMergeUnroll groups of rows per step and issues every load of the
+// step (both lse values and both float4 of each row) before it uses any, so a
+// step costs one memory round trip instead of two per row.  The row's lse is
+// read by all its lanes before lane 0 of the row writes it back (__syncwarp).
+// Idx is uint32_t when B * n * H fits, uint64_t otherwise.
+constexpr int kMergeUnroll = 4;
+constexpr int kMergeThreads = 256;
+
+template <int D, typename Idx>
+__global__ void __launch_bounds__(kMergeThreads)
+merge_kernel(float* __restrict__ out_acc, float* __restrict__ lse_acc,
+             const float* __restrict__ out_part, const float* __restrict__ lse_part, Idx H, Idx n,
+             Idx rows) {
   constexpr int kLanesPerRow = D / 4;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  constexpr int kRowsPerStep = kRowsPerWarp * kMergeUnroll;
   const int lane = threadIdx.x % 32;
   const int sub = lane / kLanesPerRow;        // which row of the warp's group
   const int q4 = lane % kLanesPerRow;         // float4 index inside the row
-  const int64_t rows = (int64_t)B * n * H;
-  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
-  const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  for (int64_t wr = warp0 * kRowsPerWarp; wr < rows; wr += warps_total * kRowsPerWarp) {
-    const int64_t rrow = wr + sub;             // row index in [B][n][H] order
-    const bool ok = rrow < rows;
-    float l1 = -INFINITY, l2 = -INFINITY;
-    int64_t li = 0;
-    if (ok) {
-      const int h = (int)(rrow % H);
-      const int64_t j = (rrow / H) % n;
-      const int b = (int)(rrow / ((int64_t)H * n));
-      li = ((int64_t)b * H + h) * n + j;
-      l1 = lse_acc[li];
-      l2 = __ldg(lse_part + li);
+  const Idx warps_total = (Idx)gridDim.x * (kMergeThreads / 32);
+  const Idx warp0 = (Idx)blockIdx.x * (kMergeThreads / 32) + threadIdx.x / 32;
+  for (Idx base = warp0 * kRowsPerStep; base < rows; base += warps_total * kRowsPerStep) {
+    float l1[kMergeUnroll], l2[kMergeUnroll];
+    float4 oa[kMergeUnroll], op[kMergeUnroll];
+    Idx li[kMergeUnroll];
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const Idx r = base + (Idx)(u * kRowsPerWarp + sub);   // row index in [B][n][H] order
+      l1[u] = -INFINITY;
+      l2[u] = -INFINITY;
+      li[u] = 0;
+      if (r < rows) {
+        const Idx h = r % H, t = r / H;
+        li[u] = (t / n * H + h) * n + t % n;
+        l1[u] = lse_acc[li[u]];
+        l2[u] = __ldg(lse_part + li[u]);
+        oa[u] = reinterpret_cast<const float4*>(out_acc + (uint64_t)r * D)[q4];
+        op[u] = __ldg(reinterpret_cast<const float4*>(out_part + (uint64_t)r * D) + q4);
+      }
     }
     __syncwarp();
-    if (ok) {
-      float4* oa = reinterpret_cast<float4*>(out_acc + rrow * D) + q4;
-      const float4 op = __ldg(reinterpret_cast<const float4*>(out_part + rrow * D) + q4);
-      if (l1 == -INFINITY && l2 == -INFINITY) {
-        *oa = make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-        const float mx = fmaxf(l1, l2);
-        const float lse = mx + logf(expf(l1 - mx) + expf(l2 - mx));
-        const float w1 = expf(l1 - lse), w2 = expf(l2 - lse);
-        float4 a = *oa;
-        a.x = w1 * a.x + w2 * op.x;
-        a.y = w1 * a.y + w2 * op.y;
-        a.z = w1 * a.z + w2 * op.z;
-        a.w = w1 * a.w + w2 * op.w;
-        *oa = a;
-        if (q4 == 0) lse_acc[li] = lse;
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const Idx r = base + (Idx)(u * kRowsPerWarp + sub);
+      if (r >= rows) continue;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool empty = l1[u] == -INFINITY && l2[u] == -INFINITY;
+      if (!empty) {
+        const float mx = fmaxf(l1[u], l2[u]);
+        const float lse = mx + logf(expf(l1[u] - mx) + expf(l2[u] - mx));
+        const float w1 = expf(l1[u] - lse), w2 = expf(l2[u] - lse);
+        o.x = w1 * oa[u].x + w2 * op[u].x;
+        o.y = w1 * oa[u].y + w2 * op[u].y;
+        o.z = w1 * oa[u].z + w2 * op[u].z;
+        o.w = w1 * oa[u].w + w2 * op[u].w;
+        if (q4 == 0) lse_acc[li[u]] = lse;
       }
+      reinterpret_cast<float4*>(out_acc + (uint64_t)r * D)[q4] = o;
     }
   }
 }

@@ -811,15 +811,36 @@ ra_status ring_attn_merge(float* out_acc, float* lse_acc, const float* out_part,
   ra_status st = device_info(&dev);
   if (st != RA_OK) return st;
   const int64_t rows = (int64_t)B * n * H;
-  const int rows_per_block = 8 * (32 / (D / 4));
+  const int64_t rows_per_block = (ra::kMergeThreads / 32) * (32 / (D / 4)) * ra::kMergeUnroll;
   int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
-  const int64_t cap = (int64_t)dev->sms * 8;
+  // 32-bit indices when every row index and every stride sum stays below 2^32
+  const bool narrow = 2 * (rows + rows_per_block) < (int64_t(1) << 32);
+  const void* fn = D == 128 ? (narrow ? (const void*)ra::merge_kernel<128, uint32_t>
+                                      : (const void*)ra::merge_kernel<128, uint64_t>)
+                            : (narrow ? (const void*)ra::merge_kernel<64, uint32_t>
+                                      : (const void*)ra::merge_kernel<64, uint64_t>);
+  // one full wave of resident blocks; each warp then strides over the rows
+  int per_sm = 0;
+  cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, ra::kMergeThreads, 0);
+  if (oe != cudaSuccess) return cuda_fail(oe, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(merge)");
+  const int64_t cap = (int64_t)dev->sms * (per_sm > 0 ? per_sm : 1);
   if (blocks > cap) blocks = cap;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (D == 128)
-    ra::merge_kernel<128><<<(unsigned)blocks, 256, 0, cs>>>(out_acc, lse_acc, out_part, lse_part, B, H, n);
-  else
-    ra::merge_kernel<64><<<(unsigned)blocks, 256, 0, cs>>>(out_acc, lse_acc, out_part, lse_part, B, H, n);
+  if (narrow) {
+    if (D == 128)
+      ra::merge_kernel<128, uint32_t><<<(unsigned)blocks, ra::kMergeThreads, 0, cs>>>(
+          out_acc, lse_acc, out_part, lse_part, (uint32_t)H, (uint32_t)n, (uint32_t)rows);
+    else
+      ra::merge_kernel<64, uint32_t><<<(unsigned)blocks, ra::kMergeThreads, 0, cs>>>(
+          out_acc, lse_acc, out_part, lse_part, (uint32_t)H, (uint32_t)n, (uint32_t)rows);
+  } else {
+    if (D == 128)
+      ra::merge_kernel<128, uint64_t><<<(unsigned)blocks, ra::kMergeThreads, 0, cs>>>(
+          out_acc, lse_acc, out_part, lse_part, (uint64_t)H, (uint64_t)n, (uint64_t)rows);
+    else
+      ra::merge_kernel<64, uint64_t><<<(unsigned)blocks, ra::kMergeThreads, 0, cs>>>(
+          out_acc, lse_acc, out_part, lse_part, (uint64_t)H, (uint64_t)n, (uint64_t)rows);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "merge_kernel launch");
   return RA_OK;
