@@ -40,7 +40,10 @@
 // Tensor memory (512 columns): S or S^T [0,128), dP or dP^T [128,256),
 // accumulators from 256 (dK/dV pass: dV [256,256+D), dK [384,384+D);
 // dQ pass: dQ [256,256+D)).  The bf16 P / dS of half x overwrite columns
-// [64x, 64x+32) of their own fp32 region after it has been read.
+// [64x, 64x+32) of their own fp32 region after it has been read.  The dQ pass
+// also keeps its unit's Q [384,384+D/2) and dO [448,448+D/2) in tensor
+// memory as the A operands of S and dP, so those products read only the key
+// or value tile from shared memory.
 #pragma once
 #include "geometry.cuh"
 #include "sm103_ptx.cuh"
@@ -83,6 +86,7 @@ struct BwdCfg {
 };
 
 constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 384;
+constexpr uint32_t kColQA = 384, kColDOA = 448;   // dQ pass: Q and dO as A operands
 
 // TMA coordinates (phase, row) of the tile at offset `off` of the segment
 // starting at position pos0 of shard `shard`, for the batch entry or sequence
@@ -379,6 +383,7 @@ struct __align__(1024) DqSmem {
   uint8_t k[BwdCfg<D>::kStages][BwdCfg<D>::kTileBytes];
   uint8_t v[BwdCfg<D>::kStages][BwdCfg<D>::kTileBytes];
   uint64_t q_full, q_empty;
+  uint64_t qt_full;   // the unit's Q and dO are in tensor memory (256 arrivals)
   uint64_t st_full[BwdCfg<D>::kStages], st_empty[BwdCfg<D>::kStages];
   uint64_t s_full[2], p_full[2];
   uint64_t acc_full, acc_empty;
@@ -386,6 +391,42 @@ struct __align__(1024) DqSmem {
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// S_x = A B_x^T with A (128 rows x D) in tensor memory as bf16 pairs, B_x the
+// 64 rows of a K-major tile in shared memory starting at row 64x.
+template <int D>
+__device__ __forceinline__ void issue_half_product_ta(uint32_t d_tmem, uint32_t a_tmem,
+                                                      uint32_t b_base, int x) {
+  constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * (kTile * 128) + (kk % 4) * 32;
+    mma_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(b_base + x * (64 * 128) + off, 16, 1024), id,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+// Row `row` of a 128 x D bf16 tile that TMA laid out with 128-byte swizzle
+// (D/64 sub-tiles; 16-byte chunk c of row r at chunk position c ^ (r % 8)),
+// into this thread's tensor-memory lane as D/2 columns of bf16 pairs: the
+// layout of an M = 128 MMA's A operand.
+template <int D>
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* src, int row, uint32_t t_dst) {
+#pragma unroll
+  for (int st = 0; st < D / 64; ++st) {
+    uint32_t r[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src + st * (kTile * 128) + row * 128 +
+                                                      ((c ^ (row & 7)) << 4));
+      r[4 * c] = v.x;
+      r[4 * c + 1] = v.y;
+      r[4 * c + 2] = v.z;
+      r[4 * c + 3] = v.w;
+    }
+    tmem_st32(t_dst + 32 * st, r);
+  }
+}
 
 // S_x (or S^T_x) = A B_x^T over the D contraction, N = 64 rows of B starting
 // at row 64x; both operands K-major (128-byte swizzle, D/64 sub-tiles).
@@ -790,7 +831,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
   if (tid == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
-    mbar_init(smem_u32(&sm.q_empty), 2);
+    mbar_init(smem_u32(&sm.q_empty), 256);
+    mbar_init(smem_u32(&sm.qt_full), 256);
     for (int i = 0; i < kSt; ++i) {
       mbar_init(smem_u32(&sm.st_full[i]), 1);
       mbar_init(smem_u32(&sm.st_empty[i]), 2);
@@ -880,10 +922,12 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       // ------------------------------------------------------------ MMA issuers
       // Issuer 0 (warp 1): S_x = Q K_x^T and dQ += dS_x K_x.
       // Issuer 1 (warp 3): dP_x = dO V_x^T.
-      // s_full, st_empty and q_empty complete when both have committed.
+      // s_full and st_empty complete when both have committed.  The A
+      // operands (Q, dO) come from tensor memory, copied there per unit by the
+      // elementwise warps (qt_full).
       const int w = warp == 1 ? 0 : 1;
       uint32_t q_ph = 0, st = 0, st_ph = 0, p_ph0 = 0, p_ph1 = 0, acc_ph = 0;
-      const uint32_t a_op = w == 0 ? smem_u32(sm.q) : smem_u32(sm.dO);
+      const uint32_t a_op = tmem + (w == 0 ? kColQA : kColDOA);
       const uint32_t prod_col = w == 0 ? kColS : kColDP;
       auto prod_b = [&](uint32_t s_) { return w == 0 ? smem_u32(sm.k[s_]) : smem_u32(sm.v[s_]); };
       for (int64_t k = 0;; ++k) {
@@ -897,13 +941,13 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         KIterB it;
         kiterb_setup(g, it, u.shard, qt.qmax);
         if (!kiterb_next(g, it)) continue;
-        if (!mbar_wait(smem_u32(&sm.q_full), q_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
+        if (!mbar_wait(smem_u32(&sm.qt_full), q_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
         q_ph ^= 1;
         if (!mbar_wait(smem_u32(&sm.st_full[st]), st_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
         tc_fence_after();
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          issue_half_product<D>(tmem + prod_col + 64 * x, a_op, prod_b(st), x);
+          issue_half_product_ta<D>(tmem + prod_col + 64 * x, a_op, prod_b(st), x);
           mma_commit(smem_u32(&sm.s_full[x]));
         }
         bool first = true;
@@ -929,7 +973,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (!mbar_wait(smem_u32(&sm.st_full[nst]), nph, RA_DEV_TIMEOUT_MMA, abort_flag))
               goto done;
             tc_fence_after();
-            issue_half_product<D>(tmem + prod_col, a_op, prod_b(nst), 0);
+            issue_half_product_ta<D>(tmem + prod_col, a_op, prod_b(nst), 0);
             mma_commit(smem_u32(&sm.s_full[0]));
           }
           // half 1
@@ -944,11 +988,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           st_ph = nph;
           first = false;
           if (!more) break;
-          issue_half_product<D>(tmem + prod_col + 64, a_op, prod_b(st), 1);
+          issue_half_product_ta<D>(tmem + prod_col + 64, a_op, prod_b(st), 1);
           mma_commit(smem_u32(&sm.s_full[1]));
         }
         if (w == 0) mma_commit(smem_u32(&sm.acc_full));
-        mma_commit(smem_u32(&sm.q_empty));
         acc_ph ^= 1;
       }
     }
@@ -960,8 +1003,27 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_addr + kColS + 64 * x;
     const uint32_t t_dp = tmem + lane_addr + kColDP + 64 * x;
+    // the A operand these warps keep in tensor memory: Q (half 0) or dO (half 1)
+    const uint32_t t_a = tmem + lane_addr + (x == 0 ? kColQA : kColDOA);
+    const uint8_t* a_src = x == 0 ? sm.q : sm.dO;
     const float sl2 = p.scale_log2;
-    uint32_t s_ph = 0, acc_ph = 0;
+    uint32_t s_ph = 0, acc_ph = 0, q_ph = 0;
+    // The previous unit's dQ rows are stored after this unit's A operands are
+    // in place, so the issuers start the next unit during that store.
+    bool owed = false, owed_ok = false;
+    int64_t owed_orow = 0;
+    auto store_dq = [&]() {
+      const uint32_t t_acc = tmem + lane_addr + kColAcc0 + x * (D / 2);
+#pragma unroll
+      for (int cch = 0; cch < D / 64; ++cch) {
+        uint32_t r[32];
+        tmem_ld32(t_acc + 32 * cch, r);
+        tmem_wait_ld();
+        if (owed_ok) store_row32_bf16(p.dq + owed_orow * D + x * (D / 2) + 32 * cch, r, p.scale);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.acc_empty));
+    };
     for (int64_t k = 0;; ++k) {
       const int64_t item = item_at(k);
       if (item >= p.num_items) break;
@@ -978,6 +1040,25 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const float nl = __ldg(p.nlse2 + vi);
       const float nd = __ldg(p.ndelta + vi);
       const float2 sl2_2 = make_float2(sl2, sl2), nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
+      // Every product of the previous unit has completed once its dQ has:
+      // only then may this unit's A operands overwrite that unit's.
+      if (owed) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_full), acc_ph,
+                                               RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
+          goto done;
+        acc_ph ^= 1;
+        tc_fence_after();
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full), q_ph, RA_DEV_TIMEOUT_SOFTMAX,
+                                             abort_flag)))
+        goto done;
+      q_ph ^= 1;
+      tile_row_to_tmem<D>(a_src, row, t_a);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.qt_full));
+      mbar_arrive(smem_u32(&sm.q_empty));
+      if (owed) store_dq();
       do {
         const int k0 = it.bt * kTile;
         const int kleft = it.seg.len - k0;
@@ -1002,25 +1083,18 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_arrive(smem_u32(&sm.p_full[x]));
         ++it.bt;
       } while (kiterb_next(g, it));
-      // ---- epilogue: half x stores dq columns [x*D/2, (x+1)*D/2), times scale
+      // ---- epilogue (deferred): half x stores dq columns [x*D/2, (x+1)*D/2), times scale
+      owed = true;
+      owed_ok = row < qt.valid;
+      owed_orow = ((int64_t)w.row_base + qpos) * g.H + w.h;
+    }
+    if (owed) {
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_full), acc_ph,
                                              RA_DEV_TIMEOUT_SOFTMAX, abort_flag)))
         goto done;
       acc_ph ^= 1;
       tc_fence_after();
-      {
-        const uint32_t t_acc = tmem + lane_addr + kColAcc0 + x * (D / 2);
-        const int64_t orow = ((int64_t)w.row_base + qpos) * g.H + w.h;
-#pragma unroll
-        for (int cch = 0; cch < D / 64; ++cch) {
-          uint32_t r[32];
-          tmem_ld32(t_acc + 32 * cch, r);
-          tmem_wait_ld();
-          if (row < qt.valid) store_row32_bf16(p.dq + orow * D + x * (D / 2) + 32 * cch, r, p.scale);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.acc_empty));
+      store_dq();
     }
   }
 
