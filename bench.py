@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -199,8 +200,9 @@ def traffic_from_profiles(w: Workload):
 
 
 # ---------------------------------------------------------------- CPU oracle leg
-def oracle_sample(w: Workload, q, k, v, rows_per_step: int, seed: int):
-    """Times the fp64 oracle on `rows_per_step` query rows (all heads)."""
+def oracle_sample(w: Workload, q, k, v, rows_per_step: int, seed: int, nthreads=None):
+    """Times the fp64 oracle on `rows_per_step` query rows (all heads), on
+    `nthreads` host threads (all cores when None)."""
     import oracle  # test infrastructure: the CPU-baseline leg only
 
     rng = np.random.default_rng(seed)
@@ -208,12 +210,12 @@ def oracle_sample(w: Workload, q, k, v, rows_per_step: int, seed: int):
     qr = q[:, torch.from_numpy(rows).to(q.device)].float().cpu().numpy().astype(np.float64)
     flops = float(sum(4.0 * w.D * ((r + 1) if w.causal else w.S) for r in rows)) * w.B * w.H
     t0 = time.perf_counter()
-    oracle.attn_fwd_rows(qr, rows, k, v, w.causal, w.scale)
+    oracle.attn_fwd_rows(qr, rows, k, v, w.causal, w.scale, nthreads=nthreads)
     dt = time.perf_counter() - t0
     return flops, dt
 
 
-def oracle_train_sample(w: Workload, q, k, v, do, prefix: int):
+def oracle_train_sample(w: Workload, q, k, v, do, prefix: int, nthreads=None):
     """Times the fp64 oracle's forward+backward on one (b, kv head) pair over
     the first `prefix` tokens (a causal prefix is a whole problem of its own)."""
     import oracle  # test infrastructure: the CPU-baseline leg only
@@ -226,13 +228,41 @@ def oracle_train_sample(w: Workload, q, k, v, do, prefix: int):
     dos = f64(do[:, :, :G])
     flops = 3.5 * 4.0 * G * prefix * prefix * w.D / (2 if w.causal else 1)
     t0 = time.perf_counter()
-    oracle.attn_fwd(qs, ks, vs, w.causal, w.scale)
-    oracle.attn_bwd(qs, ks, vs, dos, w.causal, w.scale, [(0, 0)])
+    oracle.attn_fwd(qs, ks, vs, w.causal, w.scale, nthreads=nthreads)
+    oracle.attn_bwd(qs, ks, vs, dos, w.causal, w.scale, [(0, 0)], nthreads=nthreads)
     return flops, time.perf_counter() - t0
 
 
 def host_kv(k, v):
     return (k.float().cpu().numpy().astype(np.float64), v.float().cpu().numpy().astype(np.float64))
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or "unknown"
+
+
+def one_core_baseline(w: Workload, q, k, v, do, kh, vh, prefix: int, seconds: float = 2.0):
+    """The same oracle on one host thread, over a short sample, for scale."""
+    f1, t1 = 0.0, 0.0
+    if w.backward:
+        pre = min(prefix, 1024)
+        f1, t1 = oracle_train_sample(w, q, k, v, do, pre, nthreads=1)
+        what = f"fwd+bwd of (b=0, kv head 0) over the first {pre} tokens"
+    else:
+        while t1 < seconds:
+            f, t = oracle_sample(w, q, kh, vh, 1, seed=int(t1 * 1000) + 11, nthreads=1)
+            f1 += f
+            t1 += t
+        what = f"uniform query rows x {w.B * w.H} (b,h)"
+    return {"value": f1 / t1 / 1e12, "unit": UNIT, "cores": 1,
+            "sample": f"{what}, {t1:.1f} s of fp64 C oracle on 1 thread"}
 
 
 def cores():
@@ -276,7 +306,7 @@ def run_reference(args, w: Workload, rank: int):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_of(w),
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -447,7 +477,11 @@ def run_ours(args, w: Workload, rank: int, world: int):
             sample = (f"uniform query rows x {w.B * w.H} (b,h), {t_s:.1f} s of fp64 C oracle, "
                       f"{f_s:.3g} counted flop")
         cpu = {"value": f_s / t_s / 1e12, "unit": UNIT, "cores": cores(), "kind": "oracle",
-               "sample": sample}
+               "sample": sample, "cpu_model": cpu_model()}
+        if w.backward:
+            cpu["one_core"] = one_core_baseline(w, q, k, v, do, None, None, args.ref_prefix)
+        else:
+            cpu["one_core"] = one_core_baseline(w, q, k, v, None, kh, vh, args.ref_prefix)
 
     line = {
         "metric": metric_of(w), "value": value, "unit": UNIT, "n_gpus": world,
