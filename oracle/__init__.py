@@ -66,7 +66,7 @@ def _load():
         lib.oracle_merge.restype = None
         lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i32, i32, i32, i64, i32, i32, dbl,
                                         vp, i32, vp, vp, vp, i32]
-        lib.oracle_work_census.argtypes = [i64, i32, i32, i32, i32, vp, vp]
+        lib.oracle_work_census.argtypes = [i64, i32, i32, i32, i32, i64, vp, vp, i32]
         lib.oracle_permute.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32]
         _lib = lib
     return _lib
@@ -205,12 +205,18 @@ def attn_bwd(q, k, v, dout, causal: bool, scale: float, bg_pairs, nthreads=None)
     return dq, dk, dv
 
 
-def work_census(S: int, P: int, layout, causal: bool, tile: int = 128):
-    """Brute-force per-shard (visible pairs, computed tiles); O(S^2)."""
+def work_census(S: int, P: int, layout, causal: bool, tile: int = 128, run: int = 0,
+                nthreads=None):
+    """Brute-force per-shard (visible pairs, computed tiles); O(S^2).
+
+    Tiles are ``tile`` consecutive local slots of a shard; with ``run`` > 0 no
+    tile straddles two runs of ``run`` slots (``run`` = S/(2P) keeps every tile
+    inside one zig-zag chunk).
+    """
     pairs = np.zeros(P, dtype=np.int64)
     tiles = np.zeros(P, dtype=np.int64)
-    rc = _load().oracle_work_census(S, P, _layout_id(layout), int(bool(causal)), tile,
-                                    _ptr(pairs), _ptr(tiles))
+    rc = _load().oracle_work_census(S, P, _layout_id(layout), int(bool(causal)), tile, int(run),
+                                    _ptr(pairs), _ptr(tiles), _threads(nthreads))
     if rc != 0:
         raise ValueError("oracle_work_census: bad arguments")
     return pairs, tiles

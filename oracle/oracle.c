@@ -550,34 +550,70 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
  *   pairs[r]  = number of visible (query, key) pairs whose query lives on
  *               shard r (all key blocks of the ring);
  *   tiles[r]  = number of (query tile, key tile) blocks with at least one
- *               visible pair, where a tile is `tile` consecutive local slots
- *               of one shard (the last one of a shard may be shorter).
- * O(S^2) work: meant for small S only.
+ *               visible pair.
+ * A tile is `tile` consecutive local slots of one shard.  With run > 0 the
+ * local slots are first cut into runs of `run` slots and no tile straddles two
+ * runs (the last tile of a run may be shorter): run = C gives tiles that stay
+ * inside one zig-zag chunk, which is how a kernel that loads each tile as one
+ * run of consecutive positions must cut them.  run = 0 cuts only at the end
+ * of the shard.  Threads split the shards r; each shard's counts are summed
+ * in one thread.  O(S^2) work.
  */
-int oracle_work_census(int64_t S, int P, int layout, int causal, int tile, int64_t *pairs,
-                       int64_t *tiles)
+typedef struct {
+    const int64_t *pos;
+    int64_t n, run, tiles_per_run, nt;
+    int P, causal, tile;
+    int64_t *pairs, *tiles;
+    unsigned char *seen;   /* nt * nt flags per thread slot, indexed by shard r */
+} census_ctx;
+
+static int64_t census_tile_of(const census_ctx *c, int64_t j)
 {
-    if (tile < 1) return -1;
-    int64_t *pos = malloc(sizeof(int64_t) * (size_t)S);
+    return (j / c->run) * c->tiles_per_run + (j % c->run) / c->tile;
+}
+
+static void census_item(void *vctx, int64_t r)
+{
+    census_ctx *c = (census_ctx *)vctx;
+    unsigned char *seen = c->seen + r * c->nt * c->nt;
+    int64_t npairs = 0, ntiles = 0;
+    for (int s = 0; s < c->P; ++s) {
+        memset(seen, 0, (size_t)(c->nt * c->nt));
+        for (int64_t j = 0; j < c->n; ++j) {
+            int64_t qp = c->pos[r * c->n + j];
+            int64_t tq = census_tile_of(c, j);
+            for (int64_t u = 0; u < c->n; ++u) {
+                if (c->causal && c->pos[(int64_t)s * c->n + u] > qp) continue;
+                npairs += 1;
+                seen[tq * c->nt + census_tile_of(c, u)] = 1;
+            }
+        }
+        for (int64_t t = 0; t < c->nt * c->nt; ++t) ntiles += seen[t];
+    }
+    c->pairs[r] = npairs;
+    c->tiles[r] = ntiles;
+}
+
+int oracle_work_census(int64_t S, int P, int layout, int causal, int tile, int64_t run,
+                       int64_t *pairs, int64_t *tiles, int nthreads)
+{
+    if (tile < 1 || run < 0) return -1;
+    int64_t *pos = malloc(sizeof(int64_t) * (size_t)(S > 0 ? S : 1));
     if (!pos) return -1;
     if (oracle_layout_positions(S, P, layout, pos) != 0) { free(pos); return -1; }
-    int64_t n = S / P;
-    int64_t nt = (n + tile - 1) / tile;
-    for (int r = 0; r < P; ++r) {
-        pairs[r] = 0;
-        tiles[r] = 0;
-        for (int s = 0; s < P; ++s)
-            for (int64_t a = 0; a < nt; ++a)
-                for (int64_t bt = 0; bt < nt; ++bt) {
-                    int64_t seen = 0;
-                    for (int64_t j = a * tile; j < n && j < (a + 1) * tile; ++j)
-                        for (int64_t u = bt * tile; u < n && u < (bt + 1) * tile; ++u)
-                            if (!causal || pos[(int64_t)s * n + u] <= pos[(int64_t)r * n + j])
-                                ++seen;
-                    pairs[r] += seen;
-                    if (seen > 0) tiles[r] += 1;
-                }
-    }
+    census_ctx c;
+    c.pos = pos;
+    c.n = S / P;
+    c.run = run > 0 && run < c.n ? run : c.n;
+    if (c.run < 1) c.run = 1;
+    c.tiles_per_run = (c.run + tile - 1) / tile;
+    c.nt = ((c.n + c.run - 1) / c.run) * c.tiles_per_run;
+    c.P = P; c.causal = causal; c.tile = tile;
+    c.pairs = pairs; c.tiles = tiles;
+    c.seen = malloc((size_t)(P * c.nt * c.nt > 0 ? P * c.nt * c.nt : 1));
+    if (!c.seen) { free(pos); return -1; }
+    run_items(census_item, &c, P, nthreads);
+    free(c.seen);
     free(pos);
     return 0;
 }

@@ -11,7 +11,7 @@ def max_abs(a, b) -> float:
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     both_inf = np.isneginf(a) & np.isneginf(b)
-    d = np.abs(np.where(both_inf, 0.0, a - b))
+    d = np.abs(np.where(both_inf, 0.0, a) - np.where(both_inf, 0.0, b))
     return float(np.max(d)) if d.size else 0.0
 
 

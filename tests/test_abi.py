@@ -50,18 +50,29 @@ def test_index_map_bit_exact_vs_oracle(layout, S, P):
 
 @pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("S,P", [(1024, 4), (768, 4), (512, 8), (2048, 2), (96, 3)])
+@pytest.mark.parametrize("S,P", [(1024, 4), (768, 4), (512, 8), (2048, 2), (96, 3), (4096, 8),
+                                 (3072, 8)])
 def test_census_matches_brute_force(layout, causal, S, P):
     if layout == "zigzag" and S % (2 * P):
         pytest.skip("zig-zag needs S % 2P == 0")
     pairs, tiles = api.census(S, P, layout, causal)
-    # oracle tiles are 128 local slots of a shard; the kernels' tiles never
-    # straddle a zig-zag chunk, which only differs when C % 128 != 0
-    bp, bt = oracle.work_census(S, P, layout, causal, tile=128)
+    # the library's tiles never straddle a zig-zag chunk: the brute force cuts
+    # its tiles at the chunk boundaries too (run = C)
+    run = S // (2 * P) if layout == "zigzag" else 0
+    bp, bt = oracle.work_census(S, P, layout, causal, tile=128, run=run)
     assert np.array_equal(pairs.numpy(), bp)
-    C = S // (2 * P)
-    if layout != "zigzag" or C % 128 == 0:
-        assert np.array_equal(tiles.numpy(), bt)
+    assert np.array_equal(tiles.numpy(), bt)
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "striped"])
+def test_census_matches_brute_force_at_the_headline_size(layout):
+    # the sizes bench.py reports its shard imbalance at: S = 131072, P = 16
+    S, P = 131072, 16
+    pairs, tiles = api.census(S, P, layout, True)
+    run = S // (2 * P) if layout == "zigzag" else 0
+    bp, bt = oracle.work_census(S, P, layout, True, tile=128, run=run)
+    assert np.array_equal(pairs.numpy(), bp)
+    assert np.array_equal(tiles.numpy(), bt)
 
 
 def test_census_balance_closed_forms_at_full_sizes():

@@ -349,3 +349,28 @@ def test_census_tiles_balance():
     assert tc.tolist() == [r * nt * nt + nt * (nt + 1) // 2 for r in range(P)]
     pairs, tiles = oracle.work_census(S, P, "contiguous", False, tile=tile)
     assert np.all(pairs == (S // P) * S) and np.all(tiles == P * nt * nt)
+
+
+def test_census_run_cut_tiles():
+    # tiles that may not straddle a run of `run` slots
+    S, P = 96, 4
+    C = S // (2 * P)                                   # 12
+    for layout in ("contiguous", "striped", "zigzag"):
+        # tile = 1: every visible pair is its own block
+        p1, t1 = oracle.work_census(S, P, layout, True, tile=1, run=C)
+        assert np.array_equal(p1, t1)
+        # runs that the tiles never reach across change nothing
+        a = oracle.work_census(S, P, layout, True, tile=4, run=0)
+        b = oracle.work_census(S, P, layout, True, tile=4, run=C)
+        c = oracle.work_census(S, P, layout, True, tile=4, run=S // P)
+        assert np.array_equal(a[1], b[1]) and np.array_equal(a[1], c[1])
+        assert np.array_equal(a[0], b[0])
+    # zig-zag with one tile per chunk: query chunk a sees key chunks 0..a, and
+    # shard r holds chunks r and 2P-1-r, so (r+1) + (2P-r) = 2P+1 blocks
+    _, tz = oracle.work_census(S, P, "zigzag", True, tile=C, run=C)
+    assert np.all(tz == 2 * P + 1)
+    # a ragged cut: chunks of 12 slots in tiles of 8 -> 2 tiles per chunk
+    # (8 + 4), 4 per shard; without the cut the shard's 24 slots make 3 tiles
+    _, tr = oracle.work_census(S, P, "zigzag", False, tile=8, run=C)
+    _, tn = oracle.work_census(S, P, "zigzag", False, tile=8, run=0)
+    assert np.all(tr == P * 4 * 4) and np.all(tn == P * 3 * 3)
