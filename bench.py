@@ -45,6 +45,7 @@ from ring_attention_02_b300.inputs import (HEADLINE, Workload, by_name, make_dou
 METRIC = "causal ring-attn fwd TFLOP/s (bf16, S=128k, 1 B300) and % of BF16 tensor peak"
 METRIC_TRAIN = "causal ring-attn fwd+bwd TFLOP/s (bf16, 1 B300; bwd counted as 2.5x fwd)"
 UNIT = "TFLOP/s"
+NOMINAL_BF16_TFLOPS = 2250.0   # dense bf16 tensor rate of a B300, vendor figure (context)
 
 
 def _dist():
@@ -492,7 +493,9 @@ def run_ours(args, w: Workload, rank: int, world: int):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"bf16 burst {peak_src}", "peak_sustained": peak_sus,
-                     "kernel": kernel},
+                     "frac_of_sustained": achieved / peak_sus,
+                     "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                     "nominal_peak": NOMINAL_BF16_TFLOPS, "kernel": kernel},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -568,6 +571,99 @@ def run_op(args, w: Workload, rank: int, world: int):
         metric = (f"causal ring-attn fwd over a pack of 16 documents TFLOP/s "
                   f"({total} tokens, lengths {min(lengths)}..{max(lengths)})")
         dtype = "bf16"
+    elif args.op == "sp_rank":
+        # one rank's forward compute under the two sequence-parallel schemes
+        # at R ranks (R = --sp-ranks, default min(P, Hkv): the head-sharded
+        # scheme needs Hkv % R == 0), the exchanges left out (one GPU):
+        #   ring:    R hops of ring_attn_step on shard 0 plus R-1 merges
+        #   Ulysses: the packing kernels around its two all-to-alls and the
+        #            fused forward over the whole sequence of H/R heads
+        R = args.sp_ranks or min(w.P, w.Hkv)
+        if w.S % (2 * R) or w.H % R or w.Hkv % R:
+            raise SystemExit(f"--sp-ranks {R} does not divide the workload")
+        nr = w.S // R
+        sh = lambda t: api.permute(t, w.S, R, w.layout).view(w.B, R, nr, *t.shape[2:])
+        q0 = sh(q)[:, 0].contiguous()
+        kvs = [(sh(k)[:, s_].contiguous(), sh(v)[:, s_].contiguous()) for s_ in range(R)]
+        acc_o = torch.empty((w.B, nr, w.H, w.D), dtype=torch.float32, device=dev)
+        acc_l = torch.empty((w.B, w.H, nr), dtype=torch.float32, device=dev)
+        part_o, part_l = torch.empty_like(acc_o), torch.empty_like(acc_l)
+        Hg, Hkg = w.H // R, w.Hkv // R
+        qf = torch.empty((w.B, w.S, Hg, w.D), dtype=torch.bfloat16, device=dev)
+        kf = torch.empty((w.B, w.S, Hkg, w.D), dtype=torch.bfloat16, device=dev)
+        vf = torch.empty_like(kf)
+        of = torch.empty_like(qf)
+        lf = torch.empty((w.B, Hg, w.S), dtype=torch.float32, device=dev)
+        k0, v0 = kvs[0]
+        blk_q, blk_k, blk_v = torch.empty_like(q0), torch.empty_like(k0), torch.empty_like(k0)
+        blk_o = torch.empty_like(qf)
+        out_s = torch.empty_like(q0)
+
+        def ring_rank():
+            api.step(q0, kvs[0][0], kvs[0][1], w.S, R, w.layout, 0, 0, w.causal, out=acc_o,
+                     lse=acc_l, stream=stream)
+            for t in range(1, R):
+                s_ = (-t) % R
+                api.step(q0, kvs[s_][0], kvs[s_][1], w.S, R, w.layout, 0, s_, w.causal,
+                         out=part_o, lse=part_l, stream=stream)
+                api.merge(acc_o, acc_l, part_o, part_l, stream=stream)
+
+        def ulysses_rank():
+            # send side: head groups of the local shard; receive side: the
+            # whole sequence of one head group (the all-to-all in between is
+            # the exchange, not timed here)
+            api.head_split(q0, w.B * nr, R, out=blk_q, stream=stream)
+            api.head_split(k0, w.B * nr, R, out=blk_k, stream=stream)
+            api.head_split(v0, w.B * nr, R, out=blk_v, stream=stream)
+            api.permute_shards(blk_q.view(R, w.B, nr, Hg, w.D), w.S, R, w.layout, inverse=True,
+                               out=qf, stream=stream)
+            api.permute_shards(blk_k.view(R, w.B, nr, Hkg, w.D), w.S, R, w.layout, inverse=True,
+                               out=kf, stream=stream)
+            api.permute_shards(blk_v.view(R, w.B, nr, Hkg, w.D), w.S, R, w.layout, inverse=True,
+                               out=vf, stream=stream)
+            api.fwd(qf, kf, vf, 1, "contiguous", w.causal, out=of, lse=lf, stream=stream)
+            api.permute_shards(of, w.S, R, w.layout, out=blk_o, stream=stream)
+            api.head_split(blk_o.view(R, w.B * nr, Hg * w.D), w.B * nr, R, inverse=True,
+                           out=out_s, stream=stream)
+
+        def timed(fn, reps):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / reps
+
+        with ClockSampler(local) as clk:
+            ring_ms = timed(ring_rank, args.steps)
+            uly_ms = timed(ulysses_rank, args.steps)
+        api.check_status(stream)
+        if rank != 0:
+            return
+        rank_flops = w.counted_flops() / R
+        kv_bytes = 2 * w.B * nr * w.Hkv * w.D * 2
+        line = {
+            "metric": "per-rank forward compute, ring vs head-sharded (Ulysses), ms",
+            "value": ring_ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ring_ms, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {**config_of(w), "op": args.op, "ranks": R},
+            "ring": {"ms": ring_ms, "tflops": rank_flops / (ring_ms * 1e-3) / 1e12,
+                     "calls": f"{R} ring_attn_step + {R - 1} ring_attn_merge on shard 0",
+                     "bytes_sent_per_rank": (R - 1) * kv_bytes},
+            "ulysses": {"ms": uly_ms, "tflops": rank_flops / (uly_ms * 1e-3) / 1e12,
+                        "calls": "head_split x4, permute_shards x4, ring_attn_fwd (P=1)",
+                        "bytes_sent_per_rank": (R - 1) * (w.B * nr * (2 * w.H + 2 * w.Hkv)
+                                                          * w.D * 2) // R},
+            "roofline": None, "cpu_baseline": None, "e2e": None,
+            "gpu_launches": args.steps * (2 * R - 1 + 9), "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+        return
     else:
         qs = api.permute(q, w.S, w.P, w.layout).view(w.B, w.P, n, w.H, w.D)
         ks = api.permute(k, w.S, w.P, w.layout).view(w.B, w.P, n, w.Hkv, w.D)
@@ -647,7 +743,10 @@ def main(argv=None):
                     help="training workloads: tokens of the oracle's fwd+bwd sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-tokens", type=int, default=1, help="--op decode: new tokens T")
-    ap.add_argument("--op", choices=["fwd", "permute", "merge", "step_merge", "decode", "varlen"],
+    ap.add_argument("--sp-ranks", type=int, default=0,
+                    help="--op sp_rank: ranks of the two schemes (default min(P, Hkv))")
+    ap.add_argument("--op", choices=["fwd", "permute", "merge", "step_merge", "decode", "varlen",
+                                     "sp_rank"],
                     default="fwd",
                     help="fwd: the workload's step (default); the others time one call")
     args = ap.parse_args(argv)

@@ -182,8 +182,12 @@ ra_status ring_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
  *   tiles per shard, counted per zig-zag chunk); larger problems get
  *   RA_ERR_SHAPE with a message, and should use ring_attn_bwd.
  *   No cudaMalloc, cudaMallocAsync, cudaFree or other allocating call is made.
- *   The first call on each device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
+ *   Each call outside stream capture looks up the array's device address with
+ *   the current device (so a device reset that reloads the library's module is
+ *   followed); a call made while `stream` is capturing reuses the address the
+ *   last uncaptured call found on that device.  Make the first call on each
+ *   device before any stream capture: a captured first call is refused with
+ *   RA_ERR_UNSUPPORTED.
  *   Every call shares the one array and it keeps the last call's contents;
  *   each call writes every scratch element it reads before reading it, so
  *   nothing needs clearing.  Calls whose kernels overlap on the GPU (other
@@ -209,7 +213,9 @@ ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
  *   k_cache, v_cache  [B][S][Hkv][D] bf16, natural token order
  *   out      [B][T][H][D], bf16 (RA_BF16) or fp32 (RA_F32)
  *   lse      [B][H][T] fp32, or NULL
- * Needs (H/Hkv) * T <= 16 and 1 <= T <= S, plus ring_attn_fwd's size rules.
+ * Needs (H/Hkv) * T <= 4096 and 1 <= T <= S, plus ring_attn_fwd's size rules;
+ * each group of 16 of a kv head's query rows runs as its own CTA over the
+ * same cache chunk (T > 1 covers a chunked prefill or a verify step).
  * The step reads the whole cache once: it is bound by HBM bandwidth and runs
  * on the CUDA cores.  Takes a transient fp32 workspace for the partials with
  * cudaMallocAsync / cudaFreeAsync on `stream`; returns RA_ERR_ALLOC if that
@@ -218,6 +224,23 @@ ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
 ra_status ring_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out,
                            ra_dtype out_dtype, float* lse, int B, int H, int Hkv, int T, int64_t S,
                            int D, int P, ra_layout layout, float scale, void* stream);
+
+/*
+ * ring_attn_cache_append -- writes the keys and values of T new tokens into
+ * the cache at positions pos .. pos+T-1: k_cache[b][pos+t] = k_new[b][t] and
+ * likewise v, for every kv head.  The Chinese article on long-context
+ * inference keeps the history's keys and values in a cache and reads them
+ * back instead of recomputing them; this is the write side of that cache,
+ * called before ring_attn_decode (whose S is then pos + T).
+ *   k_cache, v_cache [B][S_cap][Hkv][D] bf16, natural token order (the
+ *   layout's shards are read from it in place);
+ *   k_new, v_new [B][T][Hkv][D] bf16.
+ * Needs pos + T <= S_cap, D 64 or 128, 16-byte aligned non-overlapping
+ * buffers.  A plain copy: the bytes land unchanged.
+ */
+ra_status ring_attn_cache_append(void* k_cache, void* v_cache, const void* k_new,
+                                 const void* v_new, int B, int Hkv, int64_t S_cap, int64_t pos,
+                                 int T, int D, void* stream);
 
 /*
  * ring_attn_step -- one ring hop: the queries of shard r against the key/value
@@ -232,6 +255,36 @@ ra_status ring_attn_step(const void* q_shard, const void* k_shard, const void* v
                          float* out_part, float* lse_part, int B, int H, int Hkv, int64_t S,
                          int D, int P, ra_layout layout, int r, int s, int causal, float scale,
                          void* stream);
+
+/*
+ * ring_attn_step_bwd -- one ring hop of the backward: the queries of shard r
+ * against the key/value block of shard s only.  In the pages' ring the
+ * key/value blocks travel from rank to rank ("Tiefer Einblick"); the
+ * backward of that ring lets each block's dk/dv accumulators travel with it
+ * and keeps dq at the queries' rank.  This call computes one hop's share, with
+ * lse_shard the FINAL log-sum-exp of shard r's queries (over all blocks, as
+ * ring_attn_fwd or a full ring of ring_attn_step/merge produced it):
+ *   P = exp(scale q_r k_s^T - lse_r) (causal on global positions),
+ *   delta_r = rowsum(dout_r * out_r),  dS = P * (dout_r v_s^T - delta_r),
+ *   dq_part (+)= scale dS k_s,  dk_part (+)= scale dS^T q_r,  dv_part (+)= P^T dout_r,
+ * dk_part, dv_part summed over the H/Hkv query heads of a key/value head.
+ *   q_shard, out_shard, dout_shard [B][n][H][D] bf16 (shard r, local order);
+ *   k_shard, v_shard [B][n][Hkv][D] bf16 (block s, local order);
+ *   lse_shard [B][H][n] fp32 (shard r);
+ *   dq_part [B][n][H][D], dk_part, dv_part [B][n][Hkv][D]: fp32, every element
+ *   written (accumulate = 0) or added to (accumulate != 0).
+ * Summed over s = 0..P-1 (any order), dq_part is shard r's dq; summed over
+ * r, dk_part / dv_part are block s's dk / dv.  Same size rules as
+ * ring_attn_fwd; 16-byte aligned pointers.  Takes a transient workspace of
+ * 8 * B * H * T * 128 bytes (T = 128-slot tiles of one shard) with
+ * cudaMallocAsync / cudaFreeAsync on `stream`.
+ */
+ra_status ring_attn_step_bwd(const void* q_shard, const void* k_shard, const void* v_shard,
+                             const void* out_shard, const float* lse_shard,
+                             const void* dout_shard, float* dq_part, float* dk_part,
+                             float* dv_part, int B, int H, int Hkv, int64_t S, int D, int P,
+                             ra_layout layout, int r, int s, int causal, float scale,
+                             int accumulate, void* stream);
 
 /*
  * ring_attn_merge -- fold one partial into a running result, the online
@@ -258,6 +311,40 @@ ra_status ring_attn_merge(float* out_acc, float* lse_acc, const float* out_part,
 ra_status ring_attn_permute(const void* src, void* dst, int64_t outer, int64_t S,
                             int64_t row_bytes, int P, ra_layout layout, int inverse,
                             void* stream);
+
+/*
+ * ring_attn_permute_shards -- the same row permutation with the shard
+ * outermost: dst[r][o][j] = src[o][pos_r(j)] (inverse = 0), or the scatter
+ * back (inverse != 0), for o < outer.  Each shard's rows form one contiguous
+ * block of outer * n rows: the block an all-to-all sends to (or received from)
+ * rank r.  Used by the head-sharded scheme the SP/EP page names beside Ring
+ * Attention (Ulysses), whose all-to-all trades a sequence shard of every head
+ * for the whole sequence of a head group.  Sizes, alignment and overlap rules
+ * as ring_attn_permute; S < 2^31.
+ */
+ra_status ring_attn_permute_shards(const void* src, void* dst, int64_t outer, int64_t S,
+                                   int64_t row_bytes, int P, ra_layout layout, int inverse,
+                                   void* stream);
+
+/*
+ * ring_attn_head_split -- dst[p][row] = src[row][p] (inverse = 0) or
+ * dst[row][p] = src[p][row] (inverse != 0) for `rows` rows of `parts` chunks of
+ * chunk_bytes each.  A [B][n][H][D] tensor (rows = B*n, chunk = H/parts heads)
+ * becomes one block per head group, the block the head-sharded all-to-all
+ * sends to rank p; an lse [B][H][n] (rows = B, chunk = (H/parts)*n*4 bytes)
+ * likewise.  chunk_bytes a multiple of 4; 4-byte aligned, non-overlapping
+ * buffers (16-byte alignment and chunk sizes take the vector path).
+ */
+ra_status ring_attn_head_split(const void* src, void* dst, int64_t rows, int parts,
+                               int64_t chunk_bytes, int inverse, void* stream);
+
+/*
+ * ring_attn_finalize -- out[i] = bf16(acc[i]) for count fp32 values (count a
+ * multiple of 4; acc 16-byte and out 8-byte aligned): a rank's fp32 ring
+ * accumulator, after the last block has been folded in with ring_attn_merge,
+ * stored in the output type (the final store of the forward).
+ */
+ra_status ring_attn_finalize(const float* acc, void* out, int64_t count, void* stream);
 
 /*
  * ring_attn_index_map -- host-side layout map: pos[r*n + j] = global position
@@ -293,6 +380,18 @@ ra_status ring_attn_check_status(void* stream);
  * tested).
  */
 ra_status ring_attn_wait_selfcheck(int limit_ms, int64_t* waited_ns, void* stream);
+
+/*
+ * ring_attn_set_wait_limit -- the time limit of every kernel's bounded waits
+ * on the current device, in nanoseconds; 0 restores the default (about two
+ * seconds).  Tests of the failure path set a limit so short that the waits of
+ * an ordinary call run out: the kernels then give up, wait for their own
+ * copies and products still in flight, free their tensor memory and return,
+ * and ring_attn_check_status() reports RA_ERR_DEVICE_TIMEOUT.  Synchronous;
+ * make no call on another stream meanwhile.  The pages have no counterpart
+ * (they ask only that failures be detected and tested).
+ */
+ra_status ring_attn_set_wait_limit(int64_t limit_ns);
 
 /* ring_attn_last_error -- message for the last failing call on this host thread. */
 const char* ring_attn_last_error(void);

@@ -35,6 +35,8 @@ class RingAttnError(RuntimeError):
 def lib() -> ctypes.CDLL:
     """The loaded shared library (raises if it was not built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -55,22 +57,32 @@ def lib() -> ctypes.CDLL:
                                                i32, i32, i32, i32, i32, f32, vp]
             L.ring_attn_decode.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i64,
                                            i32, i32, i32, f32, vp]
+            L.ring_attn_cache_append.argtypes = [vp, vp, vp, vp, i32, i32, i64, i64, i32, i32, vp]
             L.ring_attn_step.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, i32, i32,
                                          i32, i32, i32, f32, vp]
+            L.ring_attn_step_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                             i64, i32, i32, i32, i32, i32, i32, f32, i32, vp]
             L.ring_attn_merge.argtypes = [vp, vp, vp, vp, i32, i32, i64, i32, vp]
             L.ring_attn_permute.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, vp]
+            L.ring_attn_permute_shards.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, vp]
+            L.ring_attn_head_split.argtypes = [vp, vp, i64, i32, i64, i32, vp]
+            L.ring_attn_finalize.argtypes = [vp, vp, i64, vp]
             L.ring_attn_index_map.argtypes = [i64, i32, i32, vp]
             L.ring_attn_census.argtypes = [i64, i32, i32, i32, vp, vp]
             L.ring_attn_check_status.argtypes = [vp]
             L.ring_attn_wait_selfcheck.argtypes = [i32, vp, vp]
+            L.ring_attn_set_wait_limit.argtypes = [i64]
             L.ring_attn_last_error.restype = ctypes.c_char_p
             L.ring_attn_version.restype = ctypes.c_char_p
             for name in ("ring_attn_fwd", "ring_attn_fwd_varlen", "ring_attn_fwd_counted",
                          "ring_attn_bwd",
                          "ring_attn_bwd_noalloc", "ring_attn_decode", "ring_attn_bwd_varlen",
-                         "ring_attn_step", "ring_attn_merge", "ring_attn_permute",
+                         "ring_attn_step", "ring_attn_step_bwd", "ring_attn_merge",
+                         "ring_attn_cache_append",
+                         "ring_attn_permute", "ring_attn_permute_shards",
+                         "ring_attn_head_split", "ring_attn_finalize",
                          "ring_attn_index_map", "ring_attn_census", "ring_attn_check_status",
-                         "ring_attn_wait_selfcheck"):
+                         "ring_attn_wait_selfcheck", "ring_attn_set_wait_limit"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -245,6 +257,18 @@ def decode(q, k_cache, v_cache, P: int, layout, scale: float | None = None,
     return out, lse
 
 
+def cache_append(k_cache, v_cache, k_new, v_new, pos: int, stream=None):
+    """Writes k_new, v_new [B,T,Hkv,D] into the caches [B,S_cap,Hkv,D] at
+    positions pos .. pos+T-1 (in place)."""
+    for t, nm in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, nm)
+    B, S_cap, Hkv, D = k_cache.shape
+    T = k_new.shape[1]
+    _check(lib().ring_attn_cache_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                                        B, Hkv, S_cap, int(pos), T, D, _stream(stream)))
+    return k_cache, v_cache
+
+
 def step(q_shard, k_shard, v_shard, S: int, P: int, layout, r: int, s: int,
          causal: bool = True, scale: float | None = None, out=None, lse=None, stream=None):
     """One ring hop in shard-local order: (out_part fp32 [B,n,H,D], lse_part [B,H,n]),
@@ -263,6 +287,31 @@ def step(q_shard, k_shard, v_shard, S: int, P: int, layout, r: int, s: int,
     return out, lse
 
 
+def step_bwd(q_shard, k_shard, v_shard, out_shard, lse_shard, dout_shard, S: int, P: int,
+             layout, r: int, s: int, causal: bool = True, scale: float | None = None,
+             dq=None, dk=None, dv=None, accumulate: bool = False, stream=None):
+    """One hop of the backward in shard-local order: fp32 (dq_part [B,n,H,D],
+    dk_part, dv_part [B,n,Hkv,D]) of shard r's queries against block s, written
+    into (or, accumulate=True, added to) dq, dk, dv when given."""
+    B, n, H, D = q_shard.shape
+    Hkv = k_shard.shape[2]
+    if scale is None:
+        scale = D ** -0.5
+    dev = q_shard.device
+    if dq is None:
+        dq = torch.empty((B, n, H, D), dtype=torch.float32, device=dev)
+    if dk is None:
+        dk = torch.empty((B, n, Hkv, D), dtype=torch.float32, device=dev)
+    if dv is None:
+        dv = torch.empty((B, n, Hkv, D), dtype=torch.float32, device=dev)
+    _check(lib().ring_attn_step_bwd(_ptr(q_shard), _ptr(k_shard), _ptr(v_shard), _ptr(out_shard),
+                                    _ptr(lse_shard), _ptr(dout_shard), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), B, H, Hkv, S, D, P, _layout(layout), r, s,
+                                    int(bool(causal)), float(scale), int(bool(accumulate)),
+                                    _stream(stream)))
+    return dq, dk, dv
+
+
 def merge(out_acc, lse_acc, out_part, lse_part, stream=None):
     """In-place LSE fold of (out_part, lse_part) into (out_acc, lse_acc)."""
     B, n, H, D = out_acc.shape
@@ -279,6 +328,34 @@ def permute(src, S: int, P: int, layout, inverse: bool = False, out=None, stream
     _check(lib().ring_attn_permute(_ptr(src), _ptr(dst), outer, S, row_bytes, P,
                                    _layout(layout), int(bool(inverse)), _stream(stream)))
     return dst
+
+
+def permute_shards(src, S: int, P: int, layout, inverse: bool = False, out=None, stream=None):
+    """Natural order [outer, S, ...] <-> shard-outer blocks [P, outer, S//P, ...]
+    (inverse=True scatters the blocks back).  Returns the destination; its
+    shape is src's (the caller views it as it needs)."""
+    outer = src.shape[1] if inverse else src.shape[0]
+    row_bytes = src.numel() * src.element_size() // (outer * S)
+    dst = torch.empty_like(src) if out is None else out
+    _check(lib().ring_attn_permute_shards(_ptr(src), _ptr(dst), outer, S, row_bytes, P,
+                                          _layout(layout), int(bool(inverse)), _stream(stream)))
+    return dst
+
+
+def head_split(src, rows: int, parts: int, inverse: bool = False, out=None, stream=None):
+    """[rows, parts, chunk] <-> [parts, rows, chunk] (bytes of src split evenly)."""
+    chunk_bytes = src.numel() * src.element_size() // (rows * parts)
+    dst = torch.empty_like(src) if out is None else out
+    _check(lib().ring_attn_head_split(_ptr(src), _ptr(dst), rows, parts, chunk_bytes,
+                                      int(bool(inverse)), _stream(stream)))
+    return dst
+
+
+def finalize(acc, out=None, stream=None):
+    """bf16 copy of an fp32 accumulator (same shape)."""
+    out = torch.empty(acc.shape, dtype=torch.bfloat16, device=acc.device) if out is None else out
+    _check(lib().ring_attn_finalize(_ptr(acc), _ptr(out), acc.numel(), _stream(stream)))
+    return out
 
 
 def index_map(S: int, P: int, layout):
@@ -310,6 +387,12 @@ def wait_selfcheck(limit_ms: int = 50, stream=None) -> int:
     waited = torch.zeros(1, dtype=torch.int64, device="cuda")
     _check(lib().ring_attn_wait_selfcheck(int(limit_ms), _ptr(waited), _stream(stream)))
     return int(waited.item())
+
+
+def set_wait_limit(limit_ns: int = 0):
+    """Sets the kernels' bounded-wait limit on the current device (0: the
+    default of about two seconds)."""
+    _check(lib().ring_attn_set_wait_limit(int(limit_ns)))
 
 
 def version() -> str:

@@ -27,6 +27,12 @@
 // dQ is produced by its own pass, so nothing is accumulated with atomics and
 // the result is deterministic; S and dP are computed twice for it.
 //
+// The same kernels also run one ring hop (kMode = BWD_STEP): the queries of
+// shard r against the key/value block of shard s only, on shard-local
+// tensors, writing or adding fp32 contributions: dq to shard r, dk / dv to
+// block s.  A ring of P ranks sums them hop by hop while the block's dk / dv
+// accumulators travel with the block.
+//
 // Roles in both tensor-core kernels (384 threads, one persistent CTA per SM):
 //   warp 0       TMA producer,
 //   warps 1, 3   tcgen05 issuers, one thread each (see each kernel); warp 1
@@ -50,6 +56,16 @@
 
 namespace ra {
 
+// What a launch covers (the kernels' kMode template argument):
+//   BWD_RING    the whole ring on natural-order tensors, bf16 gradients;
+//   BWD_VARLEN  the same over packed sequences;
+//   BWD_STEP    one ring hop: the queries of shard step_r against the key /
+//               value block of shard step_s, on shard-local tensors
+//               ([B][n][heads][D], local-slot order), fp32 gradients written
+//               or added (accumulate) into dq32 (the hop's dq contribution to
+//               shard r) and dk32 / dv32 (its dk, dv contribution to block s).
+enum { BWD_RING = 0, BWD_VARLEN = 1, BWD_STEP = 2 };
+
 struct BwdParams {
   Geo g;
   float scale;         // multiplies dq and dk
@@ -60,21 +76,39 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int64_t num_items;
-  // packed sequences (kernels instantiated with kVarlen = true only):
+  // packed sequences (BWD_VARLEN only):
   const int4* units;          // (sequence, shard, segment, tile) per unit, longest first
   const int64_t* cu_seqlens;  // token offset of each sequence, and the total
   const int64_t* vbase;       // first element of each sequence in the tile-order vectors
   int total;                  // tokens in the pack
+  // one ring hop (BWD_STEP only):
+  int step_r, step_s;
+  int accumulate;             // add into dq32 / dk32 / dv32 instead of overwriting
+  float* dq32;
+  float* dk32;
+  float* dv32;
 };
 
 // Tile-order vectors: slab (b, h, shard, seg, tile) holds 128 floats, one per
-// slot of that query tile.
+// slot of that query tile.  A hop (BWD_STEP) holds shard step_r's slabs only.
 __host__ __device__ inline int64_t vec_tile(const Geo& g, int b, int h, int shard, int seg,
                                             int tile) {
   return ((((int64_t)b * g.H + h) * g.P + shard) * g.nseg + seg) * g.ntile + tile;
 }
 __host__ __device__ inline int64_t vec_elems(const Geo& g) {
   return (int64_t)g.B * g.H * g.P * g.nseg * g.ntile * kTile;
+}
+__host__ __device__ inline int64_t vec_tile_step(const Geo& g, int b, int h, int seg, int tile) {
+  return (((int64_t)b * g.H + h) * g.nseg + seg) * g.ntile + tile;
+}
+__host__ __device__ inline int64_t vec_elems_step(const Geo& g) {
+  return (int64_t)g.B * g.H * g.nseg * g.ntile * kTile;
+}
+template <int kMode>
+__device__ __forceinline__ int64_t vec_slab(const Geo& g, int b, int h, int shard, int seg,
+                                            int tile) {
+  if constexpr (kMode == BWD_STEP) return vec_tile_step(g, b, h, seg, tile);
+  else return vec_tile(g, b, h, shard, seg, tile);
 }
 
 template <int D>
@@ -89,11 +123,17 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 384;
 constexpr uint32_t kColQA = 384, kColDOA = 448;   // dQ pass: Q and dO as A operands
 
 // TMA coordinates (phase, row) of the tile at offset `off` of the segment
-// starting at position pos0 of shard `shard`, for the batch entry or sequence
-// whose position 0 sits at token row row_base (a multiple of P).
-__device__ __forceinline__ void bwd_coords(const Geo& g, int shard, int pos0, int off,
+// (starting at position pos0 and local slot local0) of shard `shard`.  Ring
+// modes: natural order, the batch entry or sequence's position 0 at token row
+// row_base (a multiple of P).  Hop mode: shard-local order, the batch entry's
+// slot 0 at row row_base (= b * n).
+template <int kMode>
+__device__ __forceinline__ void bwd_coords(const Geo& g, int shard, int pos0, int local0, int off,
                                            int row_base, int& phase, int& row) {
-  if (g.layout == LAYOUT_STRIPED) {
+  if constexpr (kMode == BWD_STEP) {
+    phase = 0;
+    row = row_base + local0 + off;
+  } else if (g.layout == LAYOUT_STRIPED) {
     phase = shard;
     row = row_base / g.P + off;
   } else {
@@ -105,26 +145,28 @@ __device__ __forceinline__ void bwd_coords(const Geo& g, int shard, int pos0, in
 // ---------------------------------------------------------------- prep
 // delta = rowsum(dout * out) and -lse * log2(e) for every query row, in tile
 // order.  D/8 lanes share a row (16 bytes of dout and of out each).
-// Packed sequences (kVarlen): blockIdx.y is the sequence; its elements start
-// at vbase[seq], its tokens at cu_seqlens[seq], lse is [H][total].
-template <int D, bool kVarlen>
+// Packed sequences (BWD_VARLEN): blockIdx.y is the sequence; its elements
+// start at vbase[seq], its tokens at cu_seqlens[seq], lse is [H][total].
+// One hop (BWD_STEP): the rows of shard step_r only; out and dout are
+// [B][n][H][D] and lse [B][H][n] in shard-local order.
+template <int D, int kMode>
 __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ out,
                                 const __nv_bfloat16* __restrict__ dout,
                                 const float* __restrict__ lse, float* __restrict__ nlse2,
                                 float* __restrict__ ndelta, Geo g, const int64_t* cu_seqlens,
-                                const int64_t* vbase_arr, int total) {
+                                const int64_t* vbase_arr, int total, int step_r) {
   constexpr int kLanes = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanes;
   const int lane = threadIdx.x % 32;
   const int sub = lane / kLanes, piece = lane % kLanes;
   int64_t tok0 = 0, vbase = 0;
-  if constexpr (kVarlen) {
+  if constexpr (kMode == BWD_VARLEN) {
     const int seq = blockIdx.y;
     tok0 = cu_seqlens[seq];
     vbase = vbase_arr[seq];
     g = make_geo(1, g.H, g.Hkv, cu_seqlens[seq + 1] - tok0, g.P, g.layout, g.causal);
   }
-  const int64_t rows = vec_elems(g);
+  const int64_t rows = kMode == BWD_STEP ? vec_elems_step(g) : vec_elems(g);
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
   const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   for (int64_t base = warp0 * kRowsPerWarp; base < rows; base += warps_total * kRowsPerWarp) {
@@ -137,14 +179,21 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ out,
       const int i = (int)(e % kTile);
       const int tile = (int)(t % g.ntile); t /= g.ntile;
       const int seg = (int)(t % g.nseg); t /= g.nseg;
-      const int shard = (int)(t % g.P); t /= g.P;
+      int shard = step_r;
+      if constexpr (kMode != BWD_STEP) {
+        shard = (int)(t % g.P);
+        t /= g.P;
+      }
       const int h = (int)(t % g.H);
       const int b = (int)(t / g.H);
       const QTile qt = make_qtile(g, shard, seg, tile);
       if (i < qt.valid) {
         real = true;
         const int64_t pos = qt.pos0 + (int64_t)qt.stride * (qt.off + i);
-        const int64_t tok = kVarlen ? tok0 + pos : (int64_t)b * g.S + pos;
+        const int64_t slot = qt.local0 + qt.off + i;
+        int64_t tok;
+        if constexpr (kMode == BWD_STEP) tok = (int64_t)b * g.n + slot;
+        else tok = kMode == BWD_VARLEN ? tok0 + pos : (int64_t)b * g.S + pos;
         const int64_t off = (tok * g.H + h) * D + piece * 8;
         const uint4 a = __ldg(reinterpret_cast<const uint4*>(out + off));
         const uint4 c = __ldg(reinterpret_cast<const uint4*>(dout + off));
@@ -156,7 +205,8 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ out,
           acc = fmaf(fa.x, fc.x, acc);
           acc = fmaf(fa.y, fc.y, acc);
         }
-        lidx = kVarlen ? (int64_t)h * total + tok : ((int64_t)b * g.H + h) * g.S + pos;
+        if constexpr (kMode == BWD_STEP) lidx = ((int64_t)b * g.H + h) * g.n + slot;
+        else lidx = kMode == BWD_VARLEN ? (int64_t)h * total + tok : ((int64_t)b * g.H + h) * g.S + pos;
       }
     }
 #pragma unroll
@@ -233,13 +283,44 @@ __device__ __forceinline__ QUnit qunit_of(const Geo& g, int64_t item) {
   return w;
 }
 
+// One hop: the key tiles of block step_s, resp. the query tiles of shard
+// step_r, per (b, kv head) or (b, head); keys in increasing and queries in
+// decreasing position.
+__device__ __forceinline__ KUnit kunit_step(const Geo& g, int s, int64_t item) {
+  const int64_t U = (int64_t)g.nseg * g.ntile;
+  const int64_t bg = item / U;
+  const int64_t u = item % U;
+  KUnit w;
+  w.b = (int)(bg / g.Hkv);
+  w.hkv = (int)(bg % g.Hkv);
+  w.shard = s;
+  w.seg = (int)(u / g.ntile);
+  w.tile = (int)(u % g.ntile);
+  return w;
+}
+
+__device__ __forceinline__ QUnit qunit_step(const Geo& g, int r, int64_t item) {
+  const int64_t U = (int64_t)g.nseg * g.ntile;
+  const int64_t bh = item / U;
+  const int64_t u = item % U;
+  QUnit w;
+  w.b = (int)(bh / g.H);
+  w.h = (int)(bh % g.H);
+  w.shard = r;
+  w.seg = g.nseg - 1 - (int)(u / g.ntile);
+  w.tile = g.ntile - 1 - (int)(u % g.ntile);
+  return w;
+}
+
 // The unit of a work item and the geometry it runs in: the call's geometry,
 // or for packed sequences the unit's sequence's (B = 1, S = its length; items
 // are unit * Hkv + kv head, resp. unit * H + head, over the host's list).
-template <bool kVarlen>
+// row_base is the token row of the unit's batch entry or sequence: position 0
+// in the ring modes, local slot 0 (b * n) in the hop mode.
+template <int kMode>
 __device__ __forceinline__ const Geo& kunit_get(const BwdParams& p, int64_t item, KUnit& w,
                                                 Geo& gv) {
-  if constexpr (kVarlen) {
+  if constexpr (kMode == BWD_VARLEN) {
     const int64_t unit = item / p.g.Hkv;
     w.hkv = (int)(item % p.g.Hkv);
     w.b = 0;
@@ -252,6 +333,11 @@ __device__ __forceinline__ const Geo& kunit_get(const BwdParams& p, int64_t item
     w.row_base = (int)t0;
     w.vbase = __ldg(p.vbase + u4.x);
     return gv;
+  } else if constexpr (kMode == BWD_STEP) {
+    w = kunit_step(p.g, p.step_s, item);
+    w.row_base = w.b * p.g.n;
+    w.vbase = 0;
+    return p.g;
   } else {
     w = kunit_of(p.g, item);
     w.row_base = w.b * p.g.S;
@@ -260,10 +346,10 @@ __device__ __forceinline__ const Geo& kunit_get(const BwdParams& p, int64_t item
   }
 }
 
-template <bool kVarlen>
+template <int kMode>
 __device__ __forceinline__ const Geo& qunit_get(const BwdParams& p, int64_t item, QUnit& w,
                                                 Geo& gv) {
-  if constexpr (kVarlen) {
+  if constexpr (kMode == BWD_VARLEN) {
     const int64_t unit = item / p.g.H;
     w.h = (int)(item % p.g.H);
     w.b = 0;
@@ -276,6 +362,11 @@ __device__ __forceinline__ const Geo& qunit_get(const BwdParams& p, int64_t item
     w.row_base = (int)t0;
     w.vbase = __ldg(p.vbase + u4.x);
     return gv;
+  } else if constexpr (kMode == BWD_STEP) {
+    w = qunit_step(p.g, p.step_r, item);
+    w.row_base = w.b * p.g.n;
+    w.vbase = 0;
+    return p.g;
   } else {
     w = qunit_of(p.g, item);
     w.row_base = w.b * p.g.S;
@@ -287,10 +378,10 @@ __device__ __forceinline__ const Geo& qunit_get(const BwdParams& p, int64_t item
 // Query tiles a key tile meets, in ring order: for each query head of the
 // group, steps t = 0..P-1 visit shard r = (s + t) mod P; in each segment of r
 // the tiles holding a position >= kmin (all tiles without a causal mask) are a
-// suffix [a, ntile).
+// suffix [a, ntile).  A hop visits shard r0 only (t_end = 1).
 struct QIter {
-  int e, t, sq, a, a_end;
-  int r, h, hkv, s, kmin;
+  int e, t, t_end, sq, a, a_end;
+  int r, r0, h, hkv, s, kmin;
   Seg seg;
 };
 
@@ -306,11 +397,14 @@ __device__ __forceinline__ void qiter_range(const Geo& g, QIter& it) {
   }
 }
 
-__device__ __forceinline__ void qiter_setup(const Geo& g, QIter& it, int hkv, int s, int kmin) {
-  it.e = 0; it.t = 0; it.sq = 0;
+// Ring modes: r0 = s, t_end = P.  Hop mode: r0 = step_r, t_end = 1.
+__device__ __forceinline__ void qiter_setup(const Geo& g, QIter& it, int hkv, int s, int kmin,
+                                            int r0, int t_end) {
+  it.e = 0; it.t = 0; it.t_end = t_end; it.sq = 0;
   it.hkv = hkv; it.s = s; it.kmin = kmin;
   it.h = hkv * (g.H / g.Hkv);
-  it.r = s;
+  it.r0 = r0;
+  it.r = r0;
   qiter_range(g, it);
 }
 
@@ -318,12 +412,12 @@ __device__ __forceinline__ bool qiter_next(const Geo& g, QIter& it) {
   while (it.a >= it.a_end) {
     if (++it.sq >= g.nseg) {
       it.sq = 0;
-      if (++it.t >= g.P) {
+      if (++it.t >= it.t_end) {
         it.t = 0;
         if (++it.e >= g.H / g.Hkv) return false;
         it.h = it.hkv * (g.H / g.Hkv) + it.e;
       }
-      it.r = (it.s + it.t) % g.P;
+      it.r = (it.r0 + it.t) % g.P;
     }
     qiter_range(g, it);
   }
@@ -331,15 +425,18 @@ __device__ __forceinline__ bool qiter_next(const Geo& g, QIter& it) {
 }
 
 // Key tiles a query tile meets, in ring order s = (r - t) mod P; the visible
-// tiles of each key segment are a prefix (positions <= qmax).
+// tiles of each key segment are a prefix (positions <= qmax).  A hop visits
+// block s0 only (t_end = 1).
 struct KIterB {
-  int t, sk, bt, nk, s, r, qmax;
+  int t, t_end, sk, bt, nk, s, r, qmax;
   Seg seg;
 };
 
-__device__ __forceinline__ void kiterb_setup(const Geo& g, KIterB& it, int r, int qmax) {
-  it.t = 0; it.sk = 0; it.bt = 0; it.r = r; it.qmax = qmax;
-  it.s = r;
+// Ring modes: s0 = r, t_end = P.  Hop mode: s0 = step_s, t_end = 1.
+__device__ __forceinline__ void kiterb_setup(const Geo& g, KIterB& it, int r, int qmax, int s0,
+                                             int t_end) {
+  it.t = 0; it.t_end = t_end; it.sk = 0; it.bt = 0; it.r = r; it.qmax = qmax;
+  it.s = s0;
   it.seg = segment_of(g, it.s, 0);
   it.nk = visible_tiles(g, it.seg, qmax);
 }
@@ -349,13 +446,45 @@ __device__ __forceinline__ bool kiterb_next(const Geo& g, KIterB& it) {
     it.bt = 0;
     if (++it.sk >= g.nseg) {
       it.sk = 0;
-      if (++it.t >= g.P) return false;
+      if (++it.t >= it.t_end) return false;
       it.s = ring_block(g, it.r, it.t);
     }
     it.seg = segment_of(g, it.s, it.sk);
     it.nk = visible_tiles(g, it.seg, it.qmax);
   }
   return true;
+}
+
+// Iterator set-up for a launch's mode.
+template <int kMode>
+__device__ __forceinline__ void qiter_start(const BwdParams& p, const Geo& g, QIter& it, int hkv,
+                                            int s, int kmin) {
+  if constexpr (kMode == BWD_STEP) qiter_setup(g, it, hkv, s, kmin, p.step_r, 1);
+  else qiter_setup(g, it, hkv, s, kmin, s, g.P);
+}
+template <int kMode>
+__device__ __forceinline__ void kiterb_start(const BwdParams& p, const Geo& g, KIterB& it, int r,
+                                             int qmax) {
+  if constexpr (kMode == BWD_STEP) kiterb_setup(g, it, r, qmax, p.step_s, 1);
+  else kiterb_setup(g, it, r, qmax, r, g.P);
+}
+
+// Stores 32 fp32 accumulator columns of one row as fp32, times `mul`, added
+// to what the row holds when `acc` is set (one hop's contribution).
+__device__ __forceinline__ void store_row32_f32(float* dst, const uint32_t (&r)[32], float mul,
+                                                bool acc) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float4 v = make_float4(__uint_as_float(r[4 * i]) * mul, __uint_as_float(r[4 * i + 1]) * mul,
+                           __uint_as_float(r[4 * i + 2]) * mul,
+                           __uint_as_float(r[4 * i + 3]) * mul);
+    if (acc) {
+      const float4 o = d4[i];
+      v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+    }
+    d4[i] = v;
+  }
 }
 
 // ---------------------------------------------------------------- shared memory
@@ -543,7 +672,7 @@ __device__ __forceinline__ void dq_half(uint32_t t_s, uint32_t t_dp, float2 sl2,
 }
 
 // ---------------------------------------------------------------- dK / dV pass
-template <int D, bool kVarlen>
+template <int D, int kMode>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -584,6 +713,10 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
+  // The producer's positions: key/value tile loads issued (parity) and the
+  // next streamed stage with its lap parity.  At function scope so that an
+  // aborting CTA can wait for every load it issued.
+  uint32_t tkv_ph = 0, tst = 0, tst_ph = 0;
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
   auto item_at = [&](int64_t k) -> int64_t { return k * G + ((k & 1) ? (G - 1 - c) : c); };
@@ -597,24 +730,23 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       tma_prefetch_desc(&tm_do);
       const uint64_t pol_kv = policy_evict_first();
       const uint64_t pol_q = policy_evict_last();
-      uint32_t kv_ph = 0, st = 0, st_ph = 0;
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
         KUnit w;
         Geo gv;
-        const Geo& g = kunit_get<kVarlen>(p, item, w, gv);
+        const Geo& g = kunit_get<kMode>(p, item, w, gv);
         const QTile kt = make_qtile(g, w.shard, w.seg, w.tile);
         QIter it;
-        qiter_setup(g, it, w.hkv, w.shard, kt.qmin);
+        qiter_start<kMode>(p, g, it, w.hkv, w.shard, kt.qmin);
         if (!kt.valid || !qiter_next(g, it)) continue;
-        if (!mbar_wait(smem_u32(&sm.kv_empty), kv_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag)) goto done;
-        kv_ph ^= 1;
+        if (!mbar_wait(smem_u32(&sm.kv_empty), tkv_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag)) goto done;
+        tkv_ph ^= 1;
         {
           const uint32_t bar = smem_u32(&sm.kv_full);
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
           int phase, row;
-          bwd_coords(g, w.shard, kt.pos0, kt.off, w.row_base, phase, row);
+          bwd_coords<kMode>(g, w.shard, kt.pos0, kt.local0, kt.off, w.row_base, phase, row);
 #pragma unroll
           for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
             tma_load_4d(smem_u32(sm.k) + s2 * (kTile * 128), &tm_k, bar, 64 * s2, w.hkv, phase,
@@ -624,23 +756,23 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           }
         }
         do {
-          if (!mbar_wait(smem_u32(&sm.st_empty[st]), st_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
+          if (!mbar_wait(smem_u32(&sm.st_empty[tst]), tst_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
             goto done;
-          const uint32_t bar = smem_u32(&sm.st_full[st]);
+          const uint32_t bar = smem_u32(&sm.st_full[tst]);
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes + 2 * Cfg::kVecBytes);
           int phase, row;
-          bwd_coords(g, it.r, it.seg.pos0, it.a * kTile, w.row_base, phase, row);
+          bwd_coords<kMode>(g, it.r, it.seg.pos0, it.seg.local0, it.a * kTile, w.row_base, phase, row);
 #pragma unroll
           for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
-            tma_load_4d(smem_u32(sm.q[st]) + s2 * (kTile * 128), &tm_q, bar, 64 * s2, it.h, phase,
+            tma_load_4d(smem_u32(sm.q[tst]) + s2 * (kTile * 128), &tm_q, bar, 64 * s2, it.h, phase,
                         row, pol_q);
-            tma_load_4d(smem_u32(sm.dO[st]) + s2 * (kTile * 128), &tm_do, bar, 64 * s2, it.h,
+            tma_load_4d(smem_u32(sm.dO[tst]) + s2 * (kTile * 128), &tm_do, bar, 64 * s2, it.h,
                         phase, row, pol_q);
           }
-          const int64_t vt = w.vbase + vec_tile(g, w.b, it.h, it.r, it.sq, it.a) * kTile;
-          bulk_load(smem_u32(sm.nlse2[st]), p.nlse2 + vt, Cfg::kVecBytes, bar, pol_q);
-          bulk_load(smem_u32(sm.ndelta[st]), p.ndelta + vt, Cfg::kVecBytes, bar, pol_q);
-          if (++st == kSt) { st = 0; st_ph ^= 1; }
+          const int64_t vt = w.vbase + vec_slab<kMode>(g, w.b, it.h, it.r, it.sq, it.a) * kTile;
+          bulk_load(smem_u32(sm.nlse2[tst]), p.nlse2 + vt, Cfg::kVecBytes, bar, pol_q);
+          bulk_load(smem_u32(sm.ndelta[tst]), p.ndelta + vt, Cfg::kVecBytes, bar, pol_q);
+          if (++tst == kSt) { tst = 0; tst_ph ^= 1; }
           ++it.a;
         } while (qiter_next(g, it));
       }
@@ -662,10 +794,10 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (item >= p.num_items) break;
         KUnit u;
         Geo gv;
-        const Geo& g = kunit_get<kVarlen>(p, item, u, gv);
+        const Geo& g = kunit_get<kMode>(p, item, u, gv);
         const QTile kt = make_qtile(g, u.shard, u.seg, u.tile);
         QIter it;
-        qiter_setup(g, it, u.hkv, u.shard, kt.qmin);
+        qiter_start<kMode>(p, g, it, u.hkv, u.shard, kt.qmin);
         if (!kt.valid || !qiter_next(g, it)) continue;
         if (!mbar_wait(smem_u32(&sm.kv_full), kv_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
         kv_ph ^= 1;
@@ -736,11 +868,25 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       if (item >= p.num_items) break;
       KUnit w;
       Geo gv;
-      const Geo& g = kunit_get<kVarlen>(p, item, w, gv);
+      const Geo& g = kunit_get<kMode>(p, item, w, gv);
       const QTile kt = make_qtile(g, w.shard, w.seg, w.tile);
       QIter it;
-      qiter_setup(g, it, w.hkv, w.shard, kt.qmin);
-      if (!kt.valid || !qiter_next(g, it)) continue;
+      qiter_start<kMode>(p, g, it, w.hkv, w.shard, kt.qmin);
+      if (!kt.valid || !qiter_next(g, it)) {
+        // A hop's key tile that no query of shard step_r sees: its rows of the
+        // overwritten dv (half 0) / dk (half 1) are zero.  (In the ring modes
+        // every key is seen at least by its own position.)
+        if constexpr (kMode == BWD_STEP) {
+          if (!p.accumulate && row < kt.valid) {
+            float* dst = (x == 0 ? p.dv32 : p.dk32) +
+                         (((int64_t)w.row_base + kt.local0 + kt.off + row) * g.Hkv + w.hkv) * D;
+#pragma unroll
+            for (int i = 0; i < D / 4; ++i)
+              reinterpret_cast<float4*>(dst)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        continue;
+      }
       const int kpos = kt.pos0 + kt.stride * (kt.off + row);
       do {
         // The tile's geometry does not depend on S: work it out while the
@@ -779,16 +925,24 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       acc_ph ^= 1;
       tc_fence_after();
       {
-        __nv_bfloat16* dst = x == 0 ? p.dv : p.dk;
         const float mul = x == 0 ? 1.f : p.scale;
         const uint32_t t_acc = tmem + lane_addr + (x == 0 ? kColAcc0 : kColAcc1);
-        const int64_t orow = ((int64_t)w.row_base + kpos) * g.Hkv + w.hkv;
+        // natural order (ring modes) or this key's local slot (hop mode)
+        const int64_t orow = kMode == BWD_STEP
+            ? ((int64_t)w.row_base + kt.local0 + kt.off + row) * g.Hkv + w.hkv
+            : ((int64_t)w.row_base + kpos) * g.Hkv + w.hkv;
 #pragma unroll
         for (int cch = 0; cch < D / 32; ++cch) {
           uint32_t r[32];
           tmem_ld32(t_acc + 32 * cch, r);
           tmem_wait_ld();
-          if (row < kt.valid) store_row32_bf16(dst + orow * D + 32 * cch, r, mul);
+          if (row < kt.valid) {
+            if constexpr (kMode == BWD_STEP)
+              store_row32_f32((x == 0 ? p.dv32 : p.dk32) + orow * D + 32 * cch, r, mul,
+                              p.accumulate != 0);
+            else
+              store_row32_bf16((x == 0 ? p.dv : p.dk) + orow * D + 32 * cch, r, mul);
+          }
         }
       }
       tc_fence_before();
@@ -800,13 +954,21 @@ done:
   tc_fence_before();
   __syncthreads();
   if (sm.abort_flag) {
+    // Let whatever this CTA issued before the failure land before its tensor
+    // memory and shared memory go away: each issuer's products (a commit
+    // arrives once all of them are done), and every TMA load of the producer
+    // (the last phase armed on each full barrier; a barrier never armed
+    // reports parity 1 complete at once).
     if ((warp == 1 || warp == 3) && lane == 0) {
       const int w = warp == 1 ? 0 : 1;
       mma_commit(smem_u32(&sm.drain[w]));
-      mbar_wait(smem_u32(&sm.drain[w]), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
+      mbar_wait_for(smem_u32(&sm.drain[w]), 0, RA_DEV_TIMEOUT_DRAIN, kDrainLimitNs);
     }
-    const unsigned long long t0 = globaltimer();
-    while (globaltimer() - t0 < 1000000ull) {
+    if (warp == 0 && lane == 0) {
+      mbar_wait_for(smem_u32(&sm.kv_full), tkv_ph ^ 1, RA_DEV_TIMEOUT_DRAIN, kDrainLimitNs);
+      for (uint32_t i = 0; i < (uint32_t)kSt; ++i)
+        mbar_wait_for(smem_u32(&sm.st_full[i]), i < tst ? tst_ph : tst_ph ^ 1,
+                      RA_DEV_TIMEOUT_DRAIN, kDrainLimitNs);
     }
     __syncthreads();
   }
@@ -815,7 +977,7 @@ done:
 }
 
 // ---------------------------------------------------------------- dQ pass
-template <int D, bool kVarlen>
+template <int D, int kMode>
 __global__ void __launch_bounds__(384, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -857,6 +1019,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
+  // The producer's positions: query tile loads issued (parity) and the next
+  // streamed stage with its lap parity.  At function scope so that an
+  // aborting CTA can wait for every load it issued.
+  uint32_t tq_ph = 0, tst = 0, tst_ph = 0;
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
   auto item_at = [&](int64_t k) -> int64_t { return k * G + ((k & 1) ? (G - 1 - c) : c); };
@@ -870,25 +1036,24 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tma_prefetch_desc(&tm_do);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      uint32_t q_ph = 0, st = 0, st_ph = 0;
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
         QUnit w;
         Geo gv;
-        const Geo& g = qunit_get<kVarlen>(p, item, w, gv);
+        const Geo& g = qunit_get<kMode>(p, item, w, gv);
         const QTile qt = make_qtile(g, w.shard, w.seg, w.tile);
         if (!qt.valid) continue;
         KIterB it;
-        kiterb_setup(g, it, w.shard, qt.qmax);
+        kiterb_start<kMode>(p, g, it, w.shard, qt.qmax);
         if (!kiterb_next(g, it)) continue;
-        if (!mbar_wait(smem_u32(&sm.q_empty), q_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag)) goto done;
-        q_ph ^= 1;
+        if (!mbar_wait(smem_u32(&sm.q_empty), tq_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag)) goto done;
+        tq_ph ^= 1;
         {
           const uint32_t bar = smem_u32(&sm.q_full);
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
           int phase, row;
-          bwd_coords(g, w.shard, qt.pos0, qt.off, w.row_base, phase, row);
+          bwd_coords<kMode>(g, w.shard, qt.pos0, qt.local0, qt.off, w.row_base, phase, row);
 #pragma unroll
           for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
             tma_load_4d(smem_u32(sm.q) + s2 * (kTile * 128), &tm_q, bar, 64 * s2, w.h, phase, row,
@@ -899,20 +1064,20 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         const int hkv = w.h / (g.H / g.Hkv);
         do {
-          if (!mbar_wait(smem_u32(&sm.st_empty[st]), st_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
+          if (!mbar_wait(smem_u32(&sm.st_empty[tst]), tst_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
             goto done;
-          const uint32_t bar = smem_u32(&sm.st_full[st]);
+          const uint32_t bar = smem_u32(&sm.st_full[tst]);
           mbar_arrive_expect_tx(bar, 2 * Cfg::kTileBytes);
           int phase, row;
-          bwd_coords(g, it.s, it.seg.pos0, it.bt * kTile, w.row_base, phase, row);
+          bwd_coords<kMode>(g, it.s, it.seg.pos0, it.seg.local0, it.bt * kTile, w.row_base, phase, row);
 #pragma unroll
           for (int s2 = 0; s2 < Cfg::kSubTiles; ++s2) {
-            tma_load_4d(smem_u32(sm.k[st]) + s2 * (kTile * 128), &tm_k, bar, 64 * s2, hkv, phase,
+            tma_load_4d(smem_u32(sm.k[tst]) + s2 * (kTile * 128), &tm_k, bar, 64 * s2, hkv, phase,
                         row, pol_kv);
-            tma_load_4d(smem_u32(sm.v[st]) + s2 * (kTile * 128), &tm_v, bar, 64 * s2, hkv, phase,
+            tma_load_4d(smem_u32(sm.v[tst]) + s2 * (kTile * 128), &tm_v, bar, 64 * s2, hkv, phase,
                         row, pol_kv);
           }
-          if (++st == kSt) { st = 0; st_ph ^= 1; }
+          if (++tst == kSt) { tst = 0; tst_ph ^= 1; }
           ++it.bt;
         } while (kiterb_next(g, it));
       }
@@ -935,11 +1100,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (item >= p.num_items) break;
         QUnit u;
         Geo gv;
-        const Geo& g = qunit_get<kVarlen>(p, item, u, gv);
+        const Geo& g = qunit_get<kMode>(p, item, u, gv);
         const QTile qt = make_qtile(g, u.shard, u.seg, u.tile);
         if (!qt.valid) continue;
         KIterB it;
-        kiterb_setup(g, it, u.shard, qt.qmax);
+        kiterb_start<kMode>(p, g, it, u.shard, qt.qmax);
         if (!kiterb_next(g, it)) continue;
         if (!mbar_wait(smem_u32(&sm.qt_full), q_ph, RA_DEV_TIMEOUT_MMA, abort_flag)) goto done;
         q_ph ^= 1;
@@ -1019,7 +1184,13 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         uint32_t r[32];
         tmem_ld32(t_acc + 32 * cch, r);
         tmem_wait_ld();
-        if (owed_ok) store_row32_bf16(p.dq + owed_orow * D + x * (D / 2) + 32 * cch, r, p.scale);
+        if (owed_ok) {
+          if constexpr (kMode == BWD_STEP)
+            store_row32_f32(p.dq32 + owed_orow * D + x * (D / 2) + 32 * cch, r, p.scale,
+                            p.accumulate != 0);
+          else
+            store_row32_bf16(p.dq + owed_orow * D + x * (D / 2) + 32 * cch, r, p.scale);
+        }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.acc_empty));
@@ -1029,14 +1200,28 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (item >= p.num_items) break;
       QUnit w;
       Geo gv;
-      const Geo& g = qunit_get<kVarlen>(p, item, w, gv);
+      const Geo& g = qunit_get<kMode>(p, item, w, gv);
       const QTile qt = make_qtile(g, w.shard, w.seg, w.tile);
       if (!qt.valid) continue;
       KIterB it;
-      kiterb_setup(g, it, w.shard, qt.qmax);
-      if (!kiterb_next(g, it)) continue;
+      kiterb_start<kMode>(p, g, it, w.shard, qt.qmax);
+      if (!kiterb_next(g, it)) {
+        // A hop's query tile that sees no key of block step_s: its rows of an
+        // overwritten dq are zero (half x writes columns [x*D/2, (x+1)*D/2)).
+        if constexpr (kMode == BWD_STEP) {
+          if (!p.accumulate && row < qt.valid) {
+            float* dst = p.dq32 +
+                         (((int64_t)w.row_base + qt.local0 + qt.off + row) * g.H + w.h) * D +
+                         x * (D / 2);
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i)
+              reinterpret_cast<float4*>(dst)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        continue;
+      }
       const int qpos = qt.pos0 + qt.stride * (qt.off + row);
-      const int64_t vi = w.vbase + vec_tile(g, w.b, w.h, w.shard, w.seg, w.tile) * kTile + row;
+      const int64_t vi = w.vbase + vec_slab<kMode>(g, w.b, w.h, w.shard, w.seg, w.tile) * kTile + row;
       const float nl = __ldg(p.nlse2 + vi);
       const float nd = __ldg(p.ndelta + vi);
       const float2 sl2_2 = make_float2(sl2, sl2), nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
@@ -1086,7 +1271,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       // ---- epilogue (deferred): half x stores dq columns [x*D/2, (x+1)*D/2), times scale
       owed = true;
       owed_ok = row < qt.valid;
-      owed_orow = ((int64_t)w.row_base + qpos) * g.H + w.h;
+      owed_orow = kMode == BWD_STEP
+                      ? ((int64_t)w.row_base + qt.local0 + qt.off + row) * g.H + w.h
+                      : ((int64_t)w.row_base + qpos) * g.H + w.h;
     }
     if (owed) {
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_full), acc_ph,
@@ -1102,13 +1289,21 @@ done:
   tc_fence_before();
   __syncthreads();
   if (sm.abort_flag) {
+    // Let whatever this CTA issued before the failure land before its tensor
+    // memory and shared memory go away: each issuer's products (a commit
+    // arrives once all of them are done), and every TMA load of the producer
+    // (the last phase armed on each full barrier; a barrier never armed
+    // reports parity 1 complete at once).
     if ((warp == 1 || warp == 3) && lane == 0) {
       const int w = warp == 1 ? 0 : 1;
       mma_commit(smem_u32(&sm.drain[w]));
-      mbar_wait(smem_u32(&sm.drain[w]), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
+      mbar_wait_for(smem_u32(&sm.drain[w]), 0, RA_DEV_TIMEOUT_DRAIN, kDrainLimitNs);
     }
-    const unsigned long long t0 = globaltimer();
-    while (globaltimer() - t0 < 1000000ull) {
+    if (warp == 0 && lane == 0) {
+      mbar_wait_for(smem_u32(&sm.q_full), tq_ph ^ 1, RA_DEV_TIMEOUT_DRAIN, kDrainLimitNs);
+      for (uint32_t i = 0; i < (uint32_t)kSt; ++i)
+        mbar_wait_for(smem_u32(&sm.st_full[i]), i < tst ? tst_ph : tst_ph ^ 1,
+                      RA_DEV_TIMEOUT_DRAIN, kDrainLimitNs);
     }
     __syncthreads();
   }

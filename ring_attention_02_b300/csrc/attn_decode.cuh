@@ -17,8 +17,8 @@
 // shared memory by TMA, three tiles in flight per CTA.
 //
 //   decode_partial_kernel  one CTA per (chunk of 128-slot tiles of one shard
-//                          segment, b, kv head); all G*T query rows of the kv
-//                          head at once (padded to one 16-row fragment); four
+//                          segment, b, kv head, group of 16 of the kv head's
+//                          G*T query rows, the last padded); four
 //                          warps, each with 32 keys of every tile and its own
 //                          online softmax, merged at the end; writes a
 //                          normalised partial and its lse.
@@ -32,7 +32,7 @@
 
 namespace ra {
 
-constexpr int kDecodeMaxRows = 16;   // G * T query rows per CTA
+constexpr int kDecodeMaxRows = 16;   // query rows per CTA (one row group)
 constexpr int kDecodeStages = 3;     // key/value tiles in flight per CTA
 
 struct DecodeParams {
@@ -46,6 +46,7 @@ struct DecodeParams {
   float* part_o;            // [B*Hkv][chunks][rows][D]
   float* part_lse;          // [B*Hkv][chunks][rows]
   int chunks;               // chunks per (b, kv head) = P * nseg * chunks_per_seg
+  int row_groups;           // ceil(rows / kDecodeMaxRows): CTAs per chunk
 };
 
 template <int D>
@@ -102,7 +103,10 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
   const int G = g.H / g.Hkv;
   const int bk = blockIdx.y;
   const int b = bk / g.Hkv, hkv = bk % g.Hkv;
-  const int chunk = blockIdx.x;
+  // the row groups of one chunk are adjacent in the grid, so they run side by
+  // side and share the chunk's key/value tiles in L2
+  const int chunk = blockIdx.x / p.row_groups;
+  const int rg0 = (blockIdx.x % p.row_groups) * kDecodeMaxRows;   // first row of this group
   // chunk -> (shard, segment, tile range)
   const int rs = chunk / p.chunks_per_seg;
   const int shard = rs / g.nseg, seg = rs % g.nseg;
@@ -117,12 +121,13 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int s = 0; s < kDecodeStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
     fence_mbar_init();
   }
-  // query rows i = e * T + t (head hkv*G + e, token t); rows >= R are zero
+  // query rows i = e * T + t (head hkv*G + e, token t) of this row group;
+  // rows >= R are zero
   for (int idx = tid; idx < kDecodeMaxRows * D; idx += blockDim.x) {
     const int i = idx / D, d = idx % D;
     float v = 0.f;
-    if (i < R) {
-      const int e = i / p.T, t = i % p.T;
+    if (rg0 + i < R) {
+      const int e = (rg0 + i) / p.T, t = (rg0 + i) % p.T;
       v = __bfloat162float(p.q[(((int64_t)b * p.T + t) * g.H + hkv * G + e) * D + d]);
     }
     sm.q[i][d] = v;
@@ -168,8 +173,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
   // the token each of this lane's two rows belongs to (rows >= R: none)
   const int qpos0 = g.S - p.T;
-  const int lim0 = r0 < R ? qpos0 + r0 % p.T : -1;       // last visible position, row r0
-  const int lim1 = r0 + 8 < R ? qpos0 + (r0 + 8) % p.T : -1;
+  const int lim0 = rg0 + r0 < R ? qpos0 + (rg0 + r0) % p.T : -1;   // last visible position
+  const int lim1 = rg0 + r0 + 8 < R ? qpos0 + (rg0 + r0 + 8) % p.T : -1;
   float o[D / 8][4];                                       // O fragments: n-tile j = d [8j, 8j+8)
 #pragma unroll
   for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -177,11 +182,16 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
   const float sl2 = p.scale_log2;
 
   bool ok = true;
+  int failed_at = ntiles;   // the tile whose wait gave up, if one did
   for (int it = 0; it < ntiles; ++it) {
     const int st = it % kDecodeStages;
     if (tid == 0 && it + kDecodeStages - 1 < ntiles) issue(it + kDecodeStages - 1);
     ok = mbar_wait(smem_u32(&sm.full[st]), (it / kDecodeStages) & 1, RA_DEV_TIMEOUT_TMA, nullptr);
-    if (!__syncthreads_and(ok)) break;
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      failed_at = it;
+      break;
+    }
     const uint32_t kb = smem_u32(sm.k[st]), vb = smem_u32(sm.v[st]);
     const int kw = 32 * warp;                               // this warp's first key slot
     // ---- S = Q K^T for the warp's 32 keys: 4 n-tiles of 8 keys
@@ -263,11 +273,17 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
     __syncthreads();
   }
   if (!ok) {
-    // a wait gave up (status already recorded): let loads still in flight land
-    // before the shared memory goes away, then report an empty partial
-    const unsigned long long t0 = globaltimer();
-    while (globaltimer() - t0 < 1000000ull) {
+    // A wait gave up (status already recorded): the tiles issued from
+    // failed_at on may still be landing.  Wait for each on its own barrier
+    // before the shared memory is reused or given up, then report an empty
+    // partial.
+    if (tid == 0) {
+      const int issued = failed_at + kDecodeStages < ntiles ? failed_at + kDecodeStages : ntiles;
+      for (int j = failed_at; j < issued; ++j)
+        mbar_wait_for(smem_u32(&sm.full[j % kDecodeStages]), (j / kDecodeStages) & 1,
+                      RA_DEV_TIMEOUT_DRAIN, kDrainLimitNs);
     }
+    __syncthreads();
   }
   // ---- merge the four warps: rows' (m, l) and O through shared memory
 #pragma unroll
@@ -293,7 +309,8 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
   __syncthreads();
   const float* o_all = reinterpret_cast<const float*>(sm.k[0]);
   const int64_t cbase = (int64_t)bk * p.chunks + chunk;
-  for (int idx = tid; idx < R * D; idx += blockDim.x) {
+  const int Rg = R - rg0 < kDecodeMaxRows ? R - rg0 : kDecodeMaxRows;   // rows of this group
+  for (int idx = tid; idx < Rg * D; idx += blockDim.x) {
     const int i = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
@@ -309,9 +326,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
     }
     const bool has = ok && L > 0.f;
-    p.part_o[(cbase * R + i) * D + d] = has ? acc / L : 0.f;
+    p.part_o[(cbase * R + rg0 + i) * D + d] = has ? acc / L : 0.f;
     if (d == 0)
-      p.part_lse[cbase * R + i] = has ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+      p.part_lse[cbase * R + rg0 + i] = has ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
 }
 

@@ -282,6 +282,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t tmem = sm.tmem_base;
   const int sblk = step_block(p);
 
+  // The producer's positions in its rings: how many Q loads each query tile
+  // slot received (parity) and the next K / V stage with its lap parity.  At
+  // function scope so that an aborting CTA can wait for every load it issued.
+  uint32_t q_ph0 = 0, q_ph1 = 0;
+  uint32_t tk_st = 0, tk_ph = 0, tv_st = 0, tv_ph = 0;
+
   // Static "snake" assignment of the longest-first item list: round k gives
   // CTA c item k*G + c (k even) or k*G + G-1-c (k odd).
   const int64_t G = gridDim.x;
@@ -298,8 +304,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_prefetch_desc(&tm_v);
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      uint32_t q_ph0 = 0, q_ph1 = 0;
-      uint32_t kst = 0, k_ph = 0, vst = 0, v_ph = 0;
       for (int64_t k = 0;; ++k) {
         const int64_t item = item_at(k);
         if (item >= p.num_items) break;
@@ -332,24 +336,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           int phase, row;
           tile_coords(g, p, it.s, it.seg.pos0, it.seg.local0, it.bt * kTile, u.row_base, phase,
                       row);
-          if (!mbar_wait(smem_u32(&sm.k_empty[kst]), k_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
+          if (!mbar_wait(smem_u32(&sm.k_empty[tk_st]), tk_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
             goto done;
-          uint32_t bar = smem_u32(&sm.k_full[kst]);
+          uint32_t bar = smem_u32(&sm.k_full[tk_st]);
           mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
 #pragma unroll
           for (int st = 0; st < Cfg::kSubTiles; ++st)
-            tma_load_4d(smem_u32(sm.k[kst]) + st * (kTile * 128), &tm_k, bar, 64 * st, u.hkv,
+            tma_load_4d(smem_u32(sm.k[tk_st]) + st * (kTile * 128), &tm_k, bar, 64 * st, u.hkv,
                         phase, row, pol_kv);
-          if (++kst == Cfg::kKStages) { kst = 0; k_ph ^= 1; }
-          if (!mbar_wait(smem_u32(&sm.v_empty[vst]), v_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
+          if (++tk_st == Cfg::kKStages) { tk_st = 0; tk_ph ^= 1; }
+          if (!mbar_wait(smem_u32(&sm.v_empty[tv_st]), tv_ph ^ 1, RA_DEV_TIMEOUT_TMA, abort_flag))
             goto done;
-          bar = smem_u32(&sm.v_full[vst]);
+          bar = smem_u32(&sm.v_full[tv_st]);
           mbar_arrive_expect_tx(bar, Cfg::kTileBytes);
 #pragma unroll
           for (int st = 0; st < Cfg::kSubTiles; ++st)
-            tma_load_4d(smem_u32(sm.v[vst]) + st * (kTile * 128), &tm_v, bar, 64 * st, u.hkv,
+            tma_load_4d(smem_u32(sm.v[tv_st]) + st * (kTile * 128), &tm_v, bar, 64 * st, u.hkv,
                         phase, row, pol_kv);
-          if (++vst == Cfg::kVStages) { vst = 0; v_ph ^= 1; }
+          if (++tv_st == Cfg::kVStages) { tv_st = 0; tv_ph ^= 1; }
           ++it.bt;
         }
       }
@@ -694,14 +698,25 @@ done:
   tc_fence_before();
   __syncthreads();
   if (sm.abort_flag) {
-    // Let whatever was issued before the failure land before TMEM goes away.
+    // Let whatever this CTA issued before the failure land before its tensor
+    // memory and shared memory go away: each issuer's products (a commit
+    // arrives once all of them are done), and every TMA load of the producer
+    // (the last phase armed on each full barrier; a barrier never armed
+    // reports parity 1 complete at once).
     if ((warp == 1 || warp == 3) && lane == 0) {
       const int x = warp == 1 ? 0 : 1;
       mma_commit(smem_u32(&sm.drain[x]));
-      mbar_wait(smem_u32(&sm.drain[x]), 0, RA_DEV_TIMEOUT_DRAIN, nullptr);
+      mbar_wait_for(smem_u32(&sm.drain[x]), 0, RA_DEV_TIMEOUT_DRAIN, kDrainLimitNs);
     }
-    const unsigned long long t0 = globaltimer();
-    while (globaltimer() - t0 < 1000000ull) {
+    if (warp == 0 && lane == 0) {
+      mbar_wait_for(smem_u32(&sm.q_full[0]), q_ph0 ^ 1, RA_DEV_TIMEOUT_DRAIN, kDrainLimitNs);
+      mbar_wait_for(smem_u32(&sm.q_full[1]), q_ph1 ^ 1, RA_DEV_TIMEOUT_DRAIN, kDrainLimitNs);
+      for (uint32_t i = 0; i < (uint32_t)Cfg::kKStages; ++i)
+        mbar_wait_for(smem_u32(&sm.k_full[i]), i < tk_st ? tk_ph : tk_ph ^ 1, RA_DEV_TIMEOUT_DRAIN,
+                      kDrainLimitNs);
+      for (uint32_t i = 0; i < (uint32_t)Cfg::kVStages; ++i)
+        mbar_wait_for(smem_u32(&sm.v_full[i]), i < tv_st ? tv_ph : tv_ph ^ 1, RA_DEV_TIMEOUT_DRAIN,
+                      kDrainLimitNs);
     }
     __syncthreads();
   }

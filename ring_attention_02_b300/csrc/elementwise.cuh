@@ -32,6 +32,94 @@ __global__ void permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restr
   }
 }
 
+// ---------------------------------------------------------------- shard-outer permute
+// dst[r][o][j] = src[o][pos_r(j)]  (gather, inverse = 0) or the scatter back:
+// the rows of every shard r gathered into one contiguous block per shard, with
+// the `outer` slabs inside it.  This is the order an all-to-all exchanges
+// (block r goes to, or came from, rank r).  Pieces are walked in shard-outer
+// order, so the shard side is read or written contiguously.
+template <typename VEC>
+__global__ void permute_shards_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                      int64_t outer, Geo g, int64_t row_bytes, int inverse) {
+  const int64_t per_row = row_bytes / (int64_t)sizeof(VEC);
+  const int64_t total = outer * g.S * per_row;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int64_t piece = idx % per_row;
+    int64_t t = idx / per_row;
+    const int64_t j = t % g.n;
+    t /= g.n;
+    const int64_t o = t % outer;
+    const int shard = (int)(t / outer);
+    const int64_t pos = position_of(g, shard, j);
+    const int64_t shard_row = ((int64_t)shard * outer + o) * g.n + j;
+    const int64_t nat_row = o * g.S + pos;
+    const int64_t from = inverse ? shard_row : nat_row;
+    const int64_t to = inverse ? nat_row : shard_row;
+    const VEC* s = reinterpret_cast<const VEC*>(src + from * row_bytes) + piece;
+    VEC* d = reinterpret_cast<VEC*>(dst + to * row_bytes) + piece;
+    *d = __ldg(s);
+  }
+}
+
+// ---------------------------------------------------------------- head split
+// dst[p][row] = src[row][p] (inverse = 0) or dst[row][p] = src[p][row], for
+// `rows` rows of `parts` chunks of chunk_bytes each: a [B][n][H][D] tensor
+// viewed as rows = B*n of H/parts-head chunks becomes one block per head
+// group (the block sent to rank p), and back.
+template <typename VEC>
+__global__ void head_split_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                  int64_t rows, int parts, int64_t chunk_bytes, int inverse) {
+  const int64_t per_chunk = chunk_bytes / (int64_t)sizeof(VEC);
+  const int64_t total = rows * parts * per_chunk;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int64_t piece = idx % per_chunk;
+    const int64_t t = idx / per_chunk;
+    const int64_t row = t % rows;
+    const int64_t part = t / rows;
+    const int64_t split = (part * rows + row) * per_chunk + piece;
+    const int64_t merged = (row * parts + part) * per_chunk + piece;
+    const VEC* s = reinterpret_cast<const VEC*>(src);
+    VEC* d = reinterpret_cast<VEC*>(dst);
+    if (inverse) d[merged] = __ldg(s + split);
+    else d[split] = __ldg(s + merged);
+  }
+}
+
+// ---------------------------------------------------------------- finalize
+// out = bf16(acc): the ring's fp32 accumulator stored in the output type once
+// the last block has been folded in.  Four values per thread step.
+__global__ void finalize_bf16_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
+                                     int64_t quads) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < quads; i += stride) {
+    const float4 v = __ldg(acc + i);
+    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+// ---------------------------------------------------------------- cache append
+// cache[b][pos + t][:] = fresh[b][t][:] for the keys and the values of T new
+// tokens (rows of `row` 16-byte vectors): the step that keeps the history's
+// keys and values in the cache for the next decode.  blockIdx.y selects the
+// tensor (0: keys, 1: values).
+__global__ void cache_append_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                    const uint4* __restrict__ k_new,
+                                    const uint4* __restrict__ v_new, int64_t B, int64_t S_cap,
+                                    int64_t pos, int64_t T, int64_t row) {
+  uint4* dst = blockIdx.y == 0 ? k_cache : v_cache;
+  const uint4* src = blockIdx.y == 0 ? k_new : v_new;
+  const int64_t total = B * T * row;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int64_t piece = idx % row;
+    const int64_t bt = idx / row;
+    const int64_t t = bt % T, b = bt / T;
+    dst[(b * S_cap + pos + t) * row + piece] = __ldg(src + idx);
+  }
+}
+
 // ---------------------------------------------------------------- merge
 // (out_acc, lse_acc) <- fold of (out_part, lse_part), rows (b, j, h):
 //   lse = max + ln(e^(l1 - max) + e^(l2 - max)),

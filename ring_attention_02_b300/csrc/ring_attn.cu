@@ -45,7 +45,7 @@ struct DeviceInfo {
   int l2_bytes = 0;
   bool fwd_attr_set[2] = {false, false};
   bool fwd_varlen_attr_set[2] = {false, false};
-  bool bwd_attr_set[4] = {false, false, false, false};
+  bool bwd_attr_set[6] = {false, false, false, false, false, false};
   bool dec_attr_set[2] = {false, false};
 };
 std::mutex g_dev_mu;
@@ -103,8 +103,8 @@ ra_status encode_fn(EncodeTiledFn* fn) {
 // 4-d bf16 view {D, heads, phases, rows} of a token tensor whose row `R` at
 // phase `ph` starts at base + (R * phases + ph) * heads * D * 2 bytes.
 // Box {64, 1, 1, 128}, 128-byte swizzle (the layout tcgen05 descriptors use).
-ra_status make_token_map(CUtensorMap* m, const void* base, int D, int heads, int64_t phases,
-                         int64_t rows) {
+ra_status encode_token_map(CUtensorMap* m, const void* base, int D, int heads, int64_t phases,
+                           int64_t rows) {
   EncodeTiledFn fn = nullptr;
   ra_status st = encode_fn(&fn);
   if (st != RA_OK) return st;
@@ -117,6 +117,37 @@ ra_status make_token_map(CUtensorMap* m, const void* base, int D, int heads, int
                   box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return RA_OK;
+}
+
+// The encoded map depends only on (base, D, heads, phases, rows), so each host
+// thread keeps the last kMapCache maps it built: a caller that runs the same
+// tensors again (a training or serving loop) skips the encode.
+struct MapEntry {
+  const void* base;
+  int D, heads;
+  int64_t phases, rows;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 32;
+thread_local MapEntry t_maps[kMapCache];
+thread_local int t_maps_used = 0, t_maps_next = 0;
+
+ra_status make_token_map(CUtensorMap* m, const void* base, int D, int heads, int64_t phases,
+                         int64_t rows) {
+  for (int i = 0; i < t_maps_used; ++i) {
+    const MapEntry& e = t_maps[i];
+    if (e.base == base && e.D == D && e.heads == heads && e.phases == phases && e.rows == rows) {
+      *m = e.map;
+      return RA_OK;
+    }
+  }
+  ra_status st = encode_token_map(m, base, D, heads, phases, rows);
+  if (st != RA_OK) return st;
+  MapEntry& e = t_maps[t_maps_next];
+  e.base = base; e.D = D; e.heads = heads; e.phases = phases; e.rows = rows; e.map = *m;
+  t_maps_next = (t_maps_next + 1) % kMapCache;
+  if (t_maps_used < kMapCache) ++t_maps_used;
   return RA_OK;
 }
 
@@ -257,16 +288,16 @@ ra_status check_bwd(const BwdArgs& a) {
   return RA_OK;
 }
 
-template <int D, bool kVarlen>
+template <int D, int kMode>
 ra_status bwd_attrs(DeviceInfo* dev) {
   const size_t smem_kv = sizeof(ra::DkdvSmem<D>) + 1024;
   const size_t smem_q = sizeof(ra::DqSmem<D>) + 1024;
-  const int di = (D == 128 ? 1 : 0) + (kVarlen ? 2 : 0);
+  const int di = (D == 128 ? 1 : 0) + 2 * kMode;
   if (!dev->bwd_attr_set[di]) {
-    cudaError_t e = cudaFuncSetAttribute(ra::attn_bwd_dkdv_kernel<D, kVarlen>,
+    cudaError_t e = cudaFuncSetAttribute(ra::attn_bwd_dkdv_kernel<D, kMode>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dkdv smem)");
-    e = cudaFuncSetAttribute(ra::attn_bwd_dq_kernel<D, kVarlen>,
+    e = cudaFuncSetAttribute(ra::attn_bwd_dq_kernel<D, kMode>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_q);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(dq smem)");
     dev->bwd_attr_set[di] = true;
@@ -280,7 +311,7 @@ ra_status launch_bwd_d(const BwdArgs& a, float* nlse2, float* ndelta, DeviceInfo
   const size_t smem_kv = sizeof(ra::DkdvSmem<D>) + 1024;
   const size_t smem_q = sizeof(ra::DqSmem<D>) + 1024;
   {
-    ra_status st0 = bwd_attrs<D, false>(dev);
+    ra_status st0 = bwd_attrs<D, ra::BWD_RING>(dev);
     if (st0 != RA_OK) return st0;
   }
   ra::BwdParams prm;
@@ -312,22 +343,78 @@ ra_status launch_bwd_d(const BwdArgs& a, float* nlse2, float* ndelta, DeviceInfo
   int64_t blocks = (vrows + rows_per_block - 1) / rows_per_block;
   const int64_t cap = (int64_t)dev->sms * 8;
   if (blocks > cap) blocks = cap;
-  ra::bwd_prep_kernel<D, false><<<(unsigned)blocks, 256, 0, stream>>>(
+  ra::bwd_prep_kernel<D, ra::BWD_RING><<<(unsigned)blocks, 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
-      nlse2, ndelta, g, nullptr, nullptr, 0);
+      nlse2, ndelta, g, nullptr, nullptr, 0, 0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bwd_prep_kernel launch");
 
   const int64_t units = (int64_t)g.P * g.nseg * g.ntile;
   prm.num_items = units * a.B * a.Hkv;
   int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
-  ra::attn_bwd_dkdv_kernel<D, false><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
+  ra::attn_bwd_dkdv_kernel<D, ra::BWD_RING><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dkdv_kernel launch");
 
   prm.num_items = units * a.B * a.H;
   grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
-  ra::attn_bwd_dq_kernel<D, false><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
+  ra::attn_bwd_dq_kernel<D, ra::BWD_RING><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dq_kernel launch");
+  return RA_OK;
+}
+
+// One ring hop of the backward: shard r's queries against block s, fp32
+// gradient contributions written or added into dq32 / dk32 / dv32.
+template <int D>
+ra_status launch_bwd_step_d(const BwdArgs& a, int r, int s, int accumulate, float* dq32,
+                            float* dk32, float* dv32, float* nlse2, float* ndelta, DeviceInfo* dev,
+                            cudaStream_t stream) {
+  const size_t smem_kv = sizeof(ra::DkdvSmem<D>) + 1024;
+  const size_t smem_q = sizeof(ra::DqSmem<D>) + 1024;
+  {
+    ra_status st0 = bwd_attrs<D, ra::BWD_STEP>(dev);
+    if (st0 != RA_OK) return st0;
+  }
+  ra::BwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.g = ra::make_geo(a.B, a.H, a.Hkv, a.S, a.P, a.layout, a.causal ? 1 : 0);
+  prm.scale = a.scale;
+  prm.scale_log2 = a.scale * 1.4426950408889634f;
+  prm.nlse2 = nlse2;
+  prm.ndelta = ndelta;
+  prm.step_r = r;
+  prm.step_s = s;
+  prm.accumulate = accumulate ? 1 : 0;
+  prm.dq32 = dq32;
+  prm.dk32 = dk32;
+  prm.dv32 = dv32;
+  const ra::Geo& g = prm.g;
+  CUtensorMap mq, mk, mv, mdo;
+  const int64_t rows = (int64_t)a.B * g.n;    // shard-local tensors
+  ra_status st = make_token_map(&mq, a.q, D, a.H, 1, rows);
+  if (st == RA_OK) st = make_token_map(&mk, a.k, D, a.Hkv, 1, rows);
+  if (st == RA_OK) st = make_token_map(&mv, a.v, D, a.Hkv, 1, rows);
+  if (st == RA_OK) st = make_token_map(&mdo, a.dout, D, a.H, 1, rows);
+  if (st != RA_OK) return st;
+  const int64_t vrows = ra::vec_elems_step(g);
+  const int rows_per_block = 8 * (32 / (D / 8));
+  int64_t blocks = (vrows + rows_per_block - 1) / rows_per_block;
+  if (blocks > (int64_t)dev->sms * 8) blocks = (int64_t)dev->sms * 8;
+  ra::bwd_prep_kernel<D, ra::BWD_STEP><<<(unsigned)blocks, 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
+      nlse2, ndelta, g, nullptr, nullptr, 0, r);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bwd_prep_kernel launch");
+  const int64_t tiles = (int64_t)g.nseg * g.ntile;
+  prm.num_items = tiles * a.B * a.Hkv;
+  int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  ra::attn_bwd_dkdv_kernel<D, ra::BWD_STEP><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dkdv_kernel launch");
+  prm.num_items = tiles * a.B * a.H;
+  grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  ra::attn_bwd_dq_kernel<D, ra::BWD_STEP><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dq_kernel launch");
   return RA_OK;
@@ -348,21 +435,34 @@ ra_status bwd_launch(const BwdArgs& a, float* nlse2, float* ndelta, cudaStream_t
 // array instead of a cudaMallocAsync workspace.  Every GPU that loads the
 // library holds it (16 MiB) until the process exits.  Host code must never
 // pass the array's name to a kernel: on the host it is only a stand-in
-// symbol.  The device address comes from cudaGetSymbolAddress, looked up
-// once per device with that device current.
+// symbol.  The device address comes from cudaGetSymbolAddress with the device
+// current.  Outside stream capture it is looked up on every call, so a
+// context that was reset and loaded the module again is followed; while
+// `stream` is capturing, the address found by the last uncaptured call on this
+// device is used (the first call on a device must therefore come before any
+// capture).
 constexpr int64_t kFixedVecMax = int64_t(1) << 21;  // floats per vector (-lse*log2e, -delta)
 static __device__ __align__(256) float g_bwd_fixed_ws[2 * kFixedVecMax];
 
 std::mutex g_fixed_mu;
 float* g_fixed_ws_ptr[64] = {nullptr};
 
-ra_status fixed_workspace(float** out) {
+ra_status fixed_workspace(cudaStream_t stream, float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(RA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cap = cudaStreamCaptureStatusActive;   // unknown: do not call into the runtime's module state
+  }
   std::lock_guard<std::mutex> lk(g_fixed_mu);
-  if (g_fixed_ws_ptr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone || g_fixed_ws_ptr[dev] == nullptr) {
+    if (cap != cudaStreamCaptureStatusNone)
+      return fail(RA_ERR_UNSUPPORTED,
+                  "ring_attn_bwd_noalloc: the first call on device %d must come before stream "
+                  "capture (it looks up the fixed workspace's address)", dev);
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_bwd_fixed_ws);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed backward workspace)");
@@ -373,6 +473,10 @@ ra_status fixed_workspace(float** out) {
 }
 
 // ---------------------------------------------------------------- decode
+// Query rows (H/Hkv)*T per key/value head a decode call takes: groups of 16
+// rows run as separate CTAs over the same key/value chunk.
+constexpr int kDecodeRowsMax = 4096;
+
 template <int D>
 ra_status launch_decode_d(const CUtensorMap& mk, const CUtensorMap& mv, const ra::DecodeParams& prm,
                           void* out, int out_f32, float* lse, DeviceInfo* dev,
@@ -386,7 +490,7 @@ ra_status launch_decode_d(const CUtensorMap& mk, const CUtensorMap& mv, const ra
     dev->dec_attr_set[di] = true;
   }
   const ra::Geo& g = prm.g;
-  dim3 grid((unsigned)prm.chunks, (unsigned)(g.B * g.Hkv));
+  dim3 grid((unsigned)(prm.chunks * prm.row_groups), (unsigned)(g.B * g.Hkv));
   ra::decode_partial_kernel<D><<<grid, ra::kDecodeThreads, smem, stream>>>(mk, mv, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode_partial_kernel launch");
@@ -441,29 +545,29 @@ ra_status launch_bwd_varlen_d(const BwdArgs& a, const CUtensorMap& mq, const CUt
                               const CUtensorMap& mv, const CUtensorMap& mdo, ra::BwdParams prm,
                               int nseq, int64_t max_vec, int nk, int nq, DeviceInfo* dev,
                               cudaStream_t stream) {
-  ra_status st = bwd_attrs<D, true>(dev);
+  ra_status st = bwd_attrs<D, ra::BWD_VARLEN>(dev);
   if (st != RA_OK) return st;
   const size_t smem_kv = sizeof(ra::DkdvSmem<D>) + 1024;
   const size_t smem_q = sizeof(ra::DqSmem<D>) + 1024;
   const int rows_per_block = 8 * (32 / (D / 8));
   int64_t bx = (max_vec + rows_per_block - 1) / rows_per_block;
   if (bx > (int64_t)dev->sms * 8) bx = (int64_t)dev->sms * 8;
-  ra::bwd_prep_kernel<D, true><<<dim3((unsigned)bx, (unsigned)nseq), 256, 0, stream>>>(
+  ra::bwd_prep_kernel<D, ra::BWD_VARLEN><<<dim3((unsigned)bx, (unsigned)nseq), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
       const_cast<float*>(prm.nlse2), const_cast<float*>(prm.ndelta), prm.g, prm.cu_seqlens,
-      prm.vbase, prm.total);
+      prm.vbase, prm.total, 0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bwd_prep_kernel launch");
   const int4* qunits = prm.units + nk;
   prm.num_items = (int64_t)nk * a.Hkv;
   int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
-  ra::attn_bwd_dkdv_kernel<D, true><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
+  ra::attn_bwd_dkdv_kernel<D, ra::BWD_VARLEN><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dkdv_kernel launch");
   prm.units = qunits;
   prm.num_items = (int64_t)nq * a.H;
   grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
-  ra::attn_bwd_dq_kernel<D, true><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
+  ra::attn_bwd_dq_kernel<D, ra::BWD_VARLEN><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dq_kernel launch");
   return RA_OK;
@@ -713,7 +817,7 @@ ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   st = device_info(&dev);
   if (st != RA_OK) return st;
   float* ws = nullptr;
-  st = fixed_workspace(&ws);
+  st = fixed_workspace(static_cast<cudaStream_t>(stream), &ws);
   if (st != RA_OK) return st;
   return bwd_launch(a, ws, ws + kFixedVecMax, static_cast<cudaStream_t>(stream));
 }
@@ -728,9 +832,9 @@ ra_status ring_attn_decode(const void* q, const void* k_cache, const void* v_cac
   ra_status st = check_common(B, H, Hkv, S, D, P, (int)layout, scale);
   if (st != RA_OK) return st;
   if (T < 1 || T > S) return fail(RA_ERR_SHAPE, "T=%d new tokens must be in [1, S=%lld]", T, (long long)S);
-  if ((H / Hkv) * T > ra::kDecodeMaxRows)
-    return fail(RA_ERR_UNSUPPORTED, "(H/Hkv)*T = %d query rows per kv head; at most %d",
-                (H / Hkv) * T, ra::kDecodeMaxRows);
+  if ((int64_t)(H / Hkv) * T > kDecodeRowsMax)
+    return fail(RA_ERR_UNSUPPORTED, "(H/Hkv)*T = %lld query rows per kv head; at most %d",
+                (long long)(H / Hkv) * T, kDecodeRowsMax);
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return fail(RA_ERR_ALIGN, "q, k_cache, v_cache and out must be 16-byte aligned");
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(RA_ERR_ALIGN, "lse must be 4-byte aligned");
@@ -747,8 +851,10 @@ ra_status ring_attn_decode(const void* q, const void* k_cache, const void* v_cac
   prm.rows = (H / Hkv) * T;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.q = static_cast<const __nv_bfloat16*>(q);
-  // Chunks of a shard segment's 128-slot tiles: about two CTAs per SM in all.
-  const int64_t tiles = (int64_t)B * Hkv * P * g.nseg * g.ntile;
+  prm.row_groups = (prm.rows + ra::kDecodeMaxRows - 1) / ra::kDecodeMaxRows;
+  // Chunks of a shard segment's 128-slot tiles: about two CTAs per SM in all
+  // (each chunk runs one CTA per row group).
+  const int64_t tiles = (int64_t)B * Hkv * P * g.nseg * g.ntile * prm.row_groups;
   int64_t ct = (tiles + 2 * dev->sms - 1) / (2 * (int64_t)dev->sms);
   if (ct < 1) ct = 1;
   if (ct > g.ntile) ct = g.ntile;
@@ -786,6 +892,43 @@ ra_status ring_attn_decode(const void* q, const void* k_cache, const void* v_cac
   return RA_OK;
 }
 
+ra_status ring_attn_cache_append(void* k_cache, void* v_cache, const void* k_new,
+                                 const void* v_new, int B, int Hkv, int64_t S_cap, int64_t pos,
+                                 int T, int D, void* stream) {
+  if (!k_cache || !v_cache || !k_new || !v_new)
+    return fail(RA_ERR_NULL, "k_cache, v_cache, k_new and v_new must be non-NULL");
+  if (B < 1 || Hkv < 1 || T < 1 || S_cap < 1 || pos < 0)
+    return fail(RA_ERR_SHAPE, "sizes must be positive (B=%d Hkv=%d T=%d S_cap=%lld pos=%lld)", B,
+                Hkv, T, (long long)S_cap, (long long)pos);
+  if (pos + T > S_cap)
+    return fail(RA_ERR_SHAPE, "pos=%lld + T=%d exceeds the cache's %lld rows", (long long)pos, T,
+                (long long)S_cap);
+  if (D != 64 && D != 128) return fail(RA_ERR_UNSUPPORTED, "head dim D=%d (supported: 64, 128)", D);
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(RA_ERR_ALIGN, "cache and new-token pointers must be 16-byte aligned");
+  const int64_t row = (int64_t)Hkv * D * 2 / 16;   // 16-byte vectors per token row
+  const int64_t nb = (int64_t)B * T * row * 16;
+  const char* ranges[4] = {static_cast<const char*>(k_cache), static_cast<const char*>(v_cache),
+                           static_cast<const char*>(k_new), static_cast<const char*>(v_new)};
+  const int64_t lens[4] = {(int64_t)B * S_cap * row * 16, (int64_t)B * S_cap * row * 16, nb, nb};
+  for (int i = 0; i < 4; ++i)
+    for (int j = i + 1; j < 4; ++j)
+      if (ranges[i] < ranges[j] + lens[j] && ranges[j] < ranges[i] + lens[i])
+        return fail(RA_ERR_SHAPE, "cache and new-token buffers overlap");
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  const int64_t total = (int64_t)B * T * row;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > (int64_t)dev->sms * 8) blocks = (int64_t)dev->sms * 8;
+  ra::cache_append_kernel<<<dim3((unsigned)blocks, 2), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), B, S_cap, pos, T, row);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "cache_append_kernel launch");
+  return RA_OK;
+}
+
 ra_status ring_attn_step(const void* q_shard, const void* k_shard, const void* v_shard,
                          float* out_part, float* lse_part, int B, int H, int Hkv, int64_t S, int D,
                          int P, ra_layout layout, int r, int s, int causal, float scale,
@@ -795,6 +938,43 @@ ra_status ring_attn_step(const void* q_shard, const void* k_shard, const void* v
     return fail(RA_ERR_SHAPE, "shard indices r=%d s=%d outside [0, %d)", r, s, P);
   return fwd_impl(ra::FWD_MODE_STEP, q_shard, k_shard, v_shard, out_part, 1, lse_part, B, H, Hkv,
                   S, D, P, layout, causal, scale, r, s, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_step_bwd(const void* q_shard, const void* k_shard, const void* v_shard,
+                             const void* out_shard, const float* lse_shard, const void* dout_shard,
+                             float* dq_part, float* dk_part, float* dv_part, int B, int H, int Hkv,
+                             int64_t S, int D, int P, ra_layout layout, int r, int s, int causal,
+                             float scale, int accumulate, void* stream) {
+  if (!dq_part || !dk_part || !dv_part) return fail(RA_ERR_NULL, "dq_part, dk_part and dv_part must be non-NULL");
+  BwdArgs a{q_shard, k_shard, v_shard, out_shard, lse_shard, dout_shard, dq_part, dk_part, dv_part,
+            B, H, Hkv, S, D, P, (int)layout, causal, scale};
+  ra_status st = check_bwd(a);
+  if (st != RA_OK) return st;
+  if (r < 0 || r >= P || s < 0 || s >= P)
+    return fail(RA_ERR_SHAPE, "shard indices r=%d s=%d outside [0, %d)", r, s, P);
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != RA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const ra::Geo g = ra::make_geo(B, H, Hkv, S, P, (int)layout, causal ? 1 : 0);
+  const size_t vec_bytes = (size_t)ra::vec_elems_step(g) * sizeof(float);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, 2 * vec_bytes, cs);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(RA_ERR_ALLOC, "cudaMallocAsync(%zu bytes) for the hop workspace: %s",
+                2 * vec_bytes, cudaGetErrorString(e));
+  }
+  float* nlse2 = static_cast<float*>(ws);
+  float* ndelta = reinterpret_cast<float*>(static_cast<char*>(ws) + vec_bytes);
+  st = D == 128 ? launch_bwd_step_d<128>(a, r, s, accumulate, dq_part, dk_part, dv_part, nlse2,
+                                         ndelta, dev, cs)
+                : launch_bwd_step_d<64>(a, r, s, accumulate, dq_part, dk_part, dv_part, nlse2,
+                                        ndelta, dev, cs);
+  e = cudaFreeAsync(ws, cs);
+  if (st != RA_OK) return st;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(hop workspace)");
+  return RA_OK;
 }
 
 ra_status ring_attn_merge(float* out_acc, float* lse_acc, const float* out_part,
@@ -883,6 +1063,96 @@ ra_status ring_attn_permute(const void* src, void* dst, int64_t outer, int64_t S
   return RA_OK;
 }
 
+ra_status ring_attn_permute_shards(const void* src, void* dst, int64_t outer, int64_t S,
+                                   int64_t row_bytes, int P, ra_layout layout, int inverse,
+                                   void* stream) {
+  if (!src || !dst) return fail(RA_ERR_NULL, "src and dst must be non-NULL");
+  if (outer < 1 || S < 1 || P < 1 || row_bytes < 4 || row_bytes % 4 != 0)
+    return fail(RA_ERR_SHAPE, "bad permute sizes (outer=%lld S=%lld row_bytes=%lld P=%d)",
+                (long long)outer, (long long)S, (long long)row_bytes, P);
+  if ((int)layout < 0 || (int)layout > 2) return fail(RA_ERR_LAYOUT, "unknown layout %d", (int)layout);
+  if (S % P != 0) return fail(RA_ERR_LAYOUT, "S=%lld is not divisible by P=%d", (long long)S, P);
+  if (layout == RA_LAYOUT_ZIGZAG && S % (2 * (int64_t)P) != 0)
+    return fail(RA_ERR_LAYOUT, "zig-zag needs S divisible by 2P");
+  if (S > 0x7fffffffLL) return fail(RA_ERR_SHAPE, "S=%lld exceeds 2^31-1", (long long)S);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
+  if (a & 3u) return fail(RA_ERR_ALIGN, "src and dst must be 4-byte aligned");
+  const char* s8 = static_cast<const char*>(src);
+  const char* d8 = static_cast<const char*>(dst);
+  const int64_t bytes = outer * S * row_bytes;
+  if (s8 < d8 + bytes && d8 < s8 + bytes) return fail(RA_ERR_SHAPE, "src and dst overlap");
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  ra::Geo g = ra::make_geo(1, 1, 1, S, P, layout, 0);
+  const bool v16 = (a & 15u) == 0 && row_bytes % 16 == 0;
+  const int64_t pieces = outer * S * (row_bytes / (v16 ? 16 : 4));
+  int64_t blocks = (pieces + 255) / 256;
+  if (blocks > (int64_t)dev->sms * 16) blocks = (int64_t)dev->sms * 16;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (v16)
+    ra::permute_shards_kernel<uint4><<<(unsigned)blocks, 256, 0, cs>>>(
+        static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), outer, g, row_bytes, inverse);
+  else
+    ra::permute_shards_kernel<uint32_t><<<(unsigned)blocks, 256, 0, cs>>>(
+        static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), outer, g, row_bytes, inverse);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "permute_shards_kernel launch");
+  return RA_OK;
+}
+
+ra_status ring_attn_head_split(const void* src, void* dst, int64_t rows, int parts,
+                               int64_t chunk_bytes, int inverse, void* stream) {
+  if (!src || !dst) return fail(RA_ERR_NULL, "src and dst must be non-NULL");
+  if (rows < 1 || parts < 1 || chunk_bytes < 4 || chunk_bytes % 4 != 0)
+    return fail(RA_ERR_SHAPE, "bad head-split sizes (rows=%lld parts=%d chunk_bytes=%lld)",
+                (long long)rows, parts, (long long)chunk_bytes);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
+  if (a & 3u) return fail(RA_ERR_ALIGN, "src and dst must be 4-byte aligned");
+  const char* s8 = static_cast<const char*>(src);
+  const char* d8 = static_cast<const char*>(dst);
+  const int64_t bytes = rows * parts * chunk_bytes;
+  if (s8 < d8 + bytes && d8 < s8 + bytes) return fail(RA_ERR_SHAPE, "src and dst overlap");
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  const bool v16 = (a & 15u) == 0 && chunk_bytes % 16 == 0;
+  const int64_t pieces = rows * parts * (chunk_bytes / (v16 ? 16 : 4));
+  int64_t blocks = (pieces + 255) / 256;
+  if (blocks > (int64_t)dev->sms * 16) blocks = (int64_t)dev->sms * 16;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (v16)
+    ra::head_split_kernel<uint4><<<(unsigned)blocks, 256, 0, cs>>>(
+        static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), rows, parts, chunk_bytes,
+        inverse);
+  else
+    ra::head_split_kernel<uint32_t><<<(unsigned)blocks, 256, 0, cs>>>(
+        static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), rows, parts, chunk_bytes,
+        inverse);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "head_split_kernel launch");
+  return RA_OK;
+}
+
+ra_status ring_attn_finalize(const float* acc, void* out, int64_t count, void* stream) {
+  if (!acc || !out) return fail(RA_ERR_NULL, "acc and out must be non-NULL");
+  if (count < 1 || count % 4 != 0)
+    return fail(RA_ERR_SHAPE, "count=%lld must be a positive multiple of 4", (long long)count);
+  if (!aligned16(acc) || (reinterpret_cast<uintptr_t>(out) & 7u))
+    return fail(RA_ERR_ALIGN, "acc must be 16-byte and out 8-byte aligned");
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  const int64_t quads = count / 4;
+  int64_t blocks = (quads + 255) / 256;
+  if (blocks > (int64_t)dev->sms * 16) blocks = (int64_t)dev->sms * 16;
+  ra::finalize_bf16_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const float4*>(acc), static_cast<uint2*>(out), quads);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "finalize_bf16_kernel launch");
+  return RA_OK;
+}
+
 ra_status ring_attn_index_map(int64_t S, int P, ra_layout layout, int64_t* pos) {
   if (!pos) return fail(RA_ERR_NULL, "pos must be non-NULL");
   if (S < 1 || P < 1) return fail(RA_ERR_SHAPE, "S and P must be positive");
@@ -934,6 +1204,18 @@ ra_status ring_attn_check_status(void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "clearing device status");
     return fail(RA_ERR_DEVICE_TIMEOUT, "a kernel gave up on a bounded wait (status 0x%x)", word);
   }
+  return RA_OK;
+}
+
+ra_status ring_attn_set_wait_limit(int64_t limit_ns) {
+  if (limit_ns < 0 || limit_ns > 60000000000LL)
+    return fail(RA_ERR_SHAPE, "limit_ns=%lld outside [0, 6e10]", (long long)limit_ns);
+  DeviceInfo* dev = nullptr;
+  ra_status st = device_info(&dev);
+  if (st != RA_OK) return st;
+  const unsigned long long v = limit_ns == 0 ? ra::kWaitLimitNs : (unsigned long long)limit_ns;
+  cudaError_t e = cudaMemcpyToSymbol(ra::g_wait_limit_ns, &v, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "setting the wait limit");
   return RA_OK;
 }
 

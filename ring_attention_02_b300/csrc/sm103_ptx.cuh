@@ -2,7 +2,7 @@
 // the kernels use: mbarriers, TMA tensor loads, tcgen05 MMA / TMEM traffic and
 // the shared-memory matrix and instruction descriptors.
 //
-// Every wait on an mbarrier is bounded: after kWaitLimitNs of wall time the
+// Every wait on an mbarrier is bounded: after g_wait_limit_ns of wall time the
 // waiter records an error code in the device status word and returns false,
 // so a broken pipeline ends with a status the host can read instead of a hang.
 #pragma once
@@ -25,6 +25,16 @@ enum : unsigned int {
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// The kernels' wait limit, kWaitLimitNs unless ring_attn_set_wait_limit()
+// chose another (tests of the failure path make it short).  Read only when a
+// wait does not complete at once.
+__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+
+// The limit of the waits that drain a CTA's own work in flight (TMA loads,
+// tensor-core products) after an abort: fixed, and long against any such
+// operation, so that a CTA never leaves while its copies still land.
+constexpr unsigned long long kDrainLimitNs = 100000000ull;  // 100 ms
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -84,10 +94,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
                                           volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
+  const unsigned long long limit = *static_cast<volatile unsigned long long*>(&g_wait_limit_ns);
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit) {
       atomicOr(&g_dev_status, err_code);
       if (abort_flag != nullptr) *abort_flag = 1;
       return false;

@@ -123,8 +123,8 @@ def test_argument_errors_return_codes_without_gpu():
     assert rc == 2   # row_bytes not a multiple of 4
     rc, _ = _status(L.ring_attn_permute, buf, buf, 1, 256, 512, 4, 0, 0, None)
     assert rc == 2   # src and dst overlap
-    # decode: (H/Hkv)*T above 16, and T above S
-    rc, _ = _status(L.ring_attn_decode, buf, buf, buf, buf, 0, None, 1, 8, 1, 3, 256, 64, 4, 0,
+    # decode: (H/Hkv)*T above 4096, and T above S
+    rc, _ = _status(L.ring_attn_decode, buf, buf, buf, buf, 0, None, 1, 8, 1, 600, 1024, 64, 4, 0,
                     0.1, None)
     assert rc == 4
     rc, _ = _status(L.ring_attn_decode, buf, buf, buf, buf, 0, None, 1, 2, 2, 300, 256, 64, 4, 0,

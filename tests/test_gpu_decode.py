@@ -71,3 +71,39 @@ def test_million_token_cache():
 
 def test_gqa_128k_cache_four_tokens():
     _case(1, 32, 8, 131072, 128, 16, "zigzag", 4, seed=26)
+
+
+@pytest.mark.parametrize("T", [64, 128])
+def test_gqa_128k_cache_chunked_prefill(T):
+    # T new tokens at once (G*T = 256 or 512 query rows per kv head: 16 or 32
+    # row groups per cache chunk) on the 128k GQA cache
+    _case(1, 32, 8, 131072, 128, 16, "zigzag", T, seed=27)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_row_groups_with_a_ragged_last_group(layout):
+    # G*T = 4*9 = 36 rows: groups of 16, 16 and 4
+    _case(2, 8, 2, 2048, 128, 4, layout, 9, seed=28)
+
+
+def test_append_then_decode():
+    # append T new tokens' keys and values into a cache that holds S-T of them,
+    # compare the cache bit for bit with a host-side copy, then decode them
+    B, H, Hkv, S, D, P, T = 2, 8, 2, 4096, 128, 8, 16
+    q_all, k_all, v_all = make_qkv(B, H, Hkv, S, D, seed=29, device="cuda")
+    kc, vc = torch.zeros_like(k_all), torch.zeros_like(v_all)
+    kc[:, :S - T] = k_all[:, :S - T]
+    vc[:, :S - T] = v_all[:, :S - T]
+    k_new, v_new = k_all[:, S - T:].contiguous(), v_all[:, S - T:].contiguous()
+    host_k = kc.view(torch.int16).cpu().clone()
+    host_k[:, S - T:] = k_new.view(torch.int16).cpu()
+    api.cache_append(kc, vc, k_new, v_new, S - T)
+    api.check_status()
+    assert torch.equal(kc.view(torch.int16).cpu(), host_k)
+    assert torch.equal(vc.view(torch.int16), v_all.view(torch.int16))
+    q = q_all[:, S - T:].contiguous()
+    out, lse = api.decode(q, kc, vc, P, "zigzag")
+    api.check_status()
+    rows = np.arange(S - T, S, dtype=np.int64)
+    ro, rl = oracle.attn_fwd_rows(to64(q), rows, to64(k_all), to64(v_all), True, D ** -0.5)
+    assert max_abs(to64(out), ro) <= OUT_TOL and max_abs(to64(lse), rl) <= LSE_TOL

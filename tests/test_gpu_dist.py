@@ -1,0 +1,144 @@
+"""GPU parity of the multi-rank ring and the head-sharded (Ulysses) scheme
+against the CPU oracle (fp64).
+
+Each rank is its own process holding one shard, and the ranks exchange blocks
+through torch.distributed.  One GPU serves all of them: the processes share
+cuda:0 and talk over gloo, which stages every block through pinned host
+memory.  No kernel waits on another rank's kernel; the exchange happens on the
+host between launches.  Each rank's outputs (shard r of out, lse, dq, dk, dv)
+are compared with the oracle's rows of that shard.
+
+Tolerances as the fused paths: out max-abs 2e-2, lse 1e-3; gradients max-abs
+5e-2 and relative L2 1e-2 per tensor.
+"""
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import oracle
+from helpers import max_abs, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, scheme, shape, layout, q):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    from ring_attention_02_b300 import api, dist as rdist
+    from ring_attention_02_b300.inputs import make_dout, make_qkv
+
+    try:
+        torch.cuda.set_device(0)
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+        B, H, Hkv, S, D = shape
+        P = world
+        qf, kf, vf = make_qkv(B, H, Hkv, S, D, seed=51, device="cuda")
+        dof = make_dout(B, H, S, D, seed=51, device="cuda")
+        n = S // P
+        shard = lambda t: api.permute(t, S, P, layout).view(B, P, n, *t.shape[2:])[:, rank] \
+            .contiguous()
+        qs, ks, vs, dos = (shard(t) for t in (qf, kf, vf, dof))
+        comm = rdist.RingComm()
+        if scheme == "ring":
+            out, lse = rdist.ring_fwd(qs, ks, vs, S, layout, True, comm=comm)
+            dq, dk, dv = rdist.ring_bwd(qs, ks, vs, out, lse, dos, S, layout, True, comm=comm)
+        else:
+            out, lse = rdist.ulysses_fwd(qs, ks, vs, S, layout, True, comm=comm)
+            dq, dk, dv = rdist.ulysses_bwd(qs, ks, vs, out, lse, dos, S, layout, True, comm=comm)
+        api.check_status()
+        f = lambda t: t.float().cpu().numpy().astype(np.float64)
+        q.put((rank, "ok", [f(t) for t in (out, lse, dq, dk, dv)]))
+        dist.barrier()
+        dist.destroy_process_group()
+    except Exception as e:  # report instead of hanging the parent
+        q.put((rank, "error", repr(e)))
+        raise
+
+
+def _run(world, scheme, shape, layout):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, scheme, shape, layout, q))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    res = {}
+    try:
+        for _ in range(world):
+            rank, status, payload = q.get(timeout=600)
+            assert status == "ok", (rank, payload)
+            res[rank] = payload
+    finally:
+        for p in procs:
+            p.join(timeout=120)
+            if p.is_alive():
+                p.kill()
+    for p in procs:
+        assert p.exitcode == 0
+    return res
+
+
+def _check(res, world, shape, layout):
+    from ring_attention_02_b300.inputs import make_dout, make_qkv
+    B, H, Hkv, S, D = shape
+    scale = D ** -0.5
+    qf, kf, vf = make_qkv(B, H, Hkv, S, D, seed=51, device="cuda")
+    dof = make_dout(B, H, S, D, seed=51, device="cuda")
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)
+    q64, k64, v64, do64 = f(qf), f(kf), f(vf), f(dof)
+    ro, rl = oracle.attn_fwd(q64, k64, v64, True, scale)
+    pairs = [(b, g) for b in range(B) for g in range(Hkv)]
+    rq, rk, rv = oracle.attn_bwd(q64, k64, v64, do64, True, scale, pairs)
+    G = H // Hkv
+    pos = oracle.layout_positions(S, world, layout)
+    worst = {}
+    for r in range(world):
+        out, lse, dq, dk, dv = res[r]
+        p = pos[r]
+        eo, el = max_abs(out, ro[:, p]), max_abs(lse, rl[:, :, p])
+        assert eo <= 2e-2 and el <= 1e-3, (r, eo, el)
+        ours_q = np.stack([np.stack([dq[b, :, g * G + e] for e in range(G)]) for b, g in pairs])
+        ours_k = np.stack([dk[b, :, g] for b, g in pairs])
+        ours_v = np.stack([dv[b, :, g] for b, g in pairs])
+        for name, o, ref in (("dq", ours_q, rq[:, :, p]), ("dk", ours_k, rk[:, p]),
+                             ("dv", ours_v, rv[:, p])):
+            ea, er = max_abs(o, ref), rel_l2(o, ref)
+            worst[name] = max(worst.get(name, 0.0), ea)
+            assert ea <= 5e-2 and er <= 1e-2, (r, name, ea, er)
+        worst["out"] = max(worst.get("out", 0.0), eo)
+        worst["lse"] = max(worst.get("lse", 0.0), el)
+    return worst
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
+@pytest.mark.parametrize("world", [2, 3])
+def test_ring_across_processes_matches_oracle(layout, world):
+    shape = (1, 4, 2, 768 * world // 3 * 2 if world == 3 else 2048, 128)
+    res = _run(world, "ring", shape, layout)
+    worst = _check(res, world, shape, layout)
+    print(f"PARITY ring world={world} {layout} S={shape[3]}: " +
+          " ".join(f"{k}={v:.3e}" for k, v in worst.items()))
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "striped", "zigzag"])
+def test_ulysses_across_processes_matches_oracle(layout):
+    shape = (2, 4, 2, 1536, 64)
+    res = _run(2, "ulysses", shape, layout)
+    worst = _check(res, 2, shape, layout)
+    print(f"PARITY ulysses world=2 {layout}: " +
+          " ".join(f"{k}={v:.3e}" for k, v in worst.items()))

@@ -6,9 +6,9 @@ import pytest
 
 import oracle
 from ring_attention_02_b300 import api
-from ring_attention_02_b300.inputs import make_qkv
+from ring_attention_02_b300.inputs import make_dout, make_qkv
 
-from helpers import max_abs, to64
+from helpers import max_abs, rel_l2, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -34,3 +34,58 @@ def test_selfcheck_rejects_bad_limits():
         api.wait_selfcheck(0)
     with pytest.raises(api.RingAttnError):
         api.wait_selfcheck(5000)
+
+
+def _expect_timeout():
+    with pytest.raises(api.RingAttnError) as ei:
+        api.check_status()
+    assert ei.value.status == 7             # RA_ERR_DEVICE_TIMEOUT
+
+
+def test_production_kernels_give_up_and_the_next_calls_are_correct():
+    # The forward and backward kernels with a 1 us wait limit, the decode with
+    # 1 ns: their waits for TMA loads and tensor-core products run out, every CTA
+    # gives up, waits for its own loads and products in flight, frees its
+    # tensor memory and returns.  The status reports the timeout once; with
+    # the default limit back, the same calls match the oracle.
+    B, H, Hkv, S, D, P = 1, 8, 4, 4096, 128, 8
+    scale = D ** -0.5
+    q, k, v = make_qkv(B, H, Hkv, S, D, seed=61, device="cuda")
+    do = make_dout(B, H, S, D, seed=61, device="cuda")
+    api.check_status()
+    out0, lse0 = api.fwd(q, k, v, P, "zigzag", True)
+    api.check_status()
+    # the decode streams its cache: on a 64k-token cache each CTA waits for
+    # tiles that are still landing, and a 1 ns limit gives up on the first one
+    qc, kc, vc = make_qkv(1, 8, 4, 65536, D, seed=62, device="cuda")
+    try:
+        api.set_wait_limit(1000)
+        api.fwd(q, k, v, P, "zigzag", True)
+        _expect_timeout()
+        api.bwd(q, k, v, out0, lse0, do, P, "zigzag", True)
+        _expect_timeout()
+        api.set_wait_limit(1)
+        api.decode(qc[:, -2:].contiguous(), kc, vc, P, "zigzag")
+        _expect_timeout()
+    finally:
+        api.set_wait_limit(0)
+    api.check_status()                      # reported once, then cleared
+    out, lse = api.fwd(q, k, v, P, "zigzag", True)
+    dq, dk, dv = api.bwd(q, k, v, out, lse, do, P, "zigzag", True)
+    od, ld = api.decode(q[:, S - 2:].contiguous(), k, v, P, "zigzag")
+    api.check_status()
+    q64, k64, v64 = to64(q), to64(k), to64(v)
+    ro, rl = oracle.attn_fwd(q64, k64, v64, True, scale)
+    assert max_abs(to64(out), ro) <= 2e-2 and max_abs(to64(lse), rl) <= 1e-3
+    assert max_abs(to64(od), ro[:, S - 2:]) <= 2e-2 and max_abs(to64(ld), rl[:, :, S - 2:]) <= 1e-3
+    rq, rk, rv = oracle.attn_bwd(q64, k64, v64, to64(do), True, scale, [(0, 1)])
+    G = H // Hkv
+    ours = (np.stack([to64(dq)[0, :, G + e] for e in range(G)]), to64(dk)[0, :, 1],
+            to64(dv)[0, :, 1])
+    for o, r in zip(ours, (rq[0], rk[0], rv[0])):
+        assert max_abs(o, r) <= 5e-2 and rel_l2(o, r) <= 1e-2
+
+
+def test_wait_limit_rejects_bad_values():
+    with pytest.raises(api.RingAttnError):
+        api.set_wait_limit(-1)
