@@ -132,6 +132,23 @@ ra_status ring_attn_fwd_counted(const void* q, const void* k, const void* v, voi
                                 float scale, int64_t* shard_tiles, void* stream);
 
 /*
+ * ring_attn_fwd_traced -- ring_attn_fwd that also records a timeline of its
+ * work items (a pair of 128-row query tiles of one shard, batch entry and
+ * head): records[4*i .. 4*i+3] = the %globaltimer (ns) when a CTA took item i
+ * up, when its last output row was stored, (shard << 32) | CTA index, and the
+ * number of key tiles its query tiles multiplied.  Grouped by shard, the
+ * records show per-rank busy time: the load balance that "Zig Zag Ring
+ * Attention" sets out to fix, measured rather than counted.
+ *   records: device int64, 8-byte aligned, at least 4 * *items words; the call
+ *   clears it on `stream` first.  capacity: records it holds (in items).
+ *   items: host int64, receives the number of work items of this call.
+ */
+ra_status ring_attn_fwd_traced(const void* q, const void* k, const void* v, void* out,
+                               ra_dtype out_dtype, float* lse, int B, int H, int Hkv, int64_t S,
+                               int D, int P, ra_layout layout, int causal, float scale,
+                               int64_t* records, int64_t capacity, int64_t* items, void* stream);
+
+/*
  * ring_attn_bwd -- gradients of ring_attn_fwd (the pages describe the forward
  * only; this is the standard softmax-attention gradient):
  *   P = exp(scale q k^T - lse), delta = rowsum(dout * out),

@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
                                                i32, i32, i32, f32, vp]
             L.ring_attn_fwd_counted.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i64, i32,
                                                 i32, i32, i32, f32, vp, vp]
+            L.ring_attn_fwd_traced.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i64, i32,
+                                               i32, i32, i32, f32, vp, i64, vp, vp]
             L.ring_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64,
                                         i32, i32, i32, i32, f32, vp]
             L.ring_attn_bwd_noalloc.argtypes = L.ring_attn_bwd.argtypes
@@ -75,6 +77,7 @@ def lib() -> ctypes.CDLL:
             L.ring_attn_last_error.restype = ctypes.c_char_p
             L.ring_attn_version.restype = ctypes.c_char_p
             for name in ("ring_attn_fwd", "ring_attn_fwd_varlen", "ring_attn_fwd_counted",
+                         "ring_attn_fwd_traced",
                          "ring_attn_bwd",
                          "ring_attn_bwd_noalloc", "ring_attn_decode", "ring_attn_bwd_varlen",
                          "ring_attn_step", "ring_attn_step_bwd", "ring_attn_merge",
@@ -178,6 +181,31 @@ def fwd_counted(q, k, v, P: int, layout, causal: bool = True, scale: float | Non
                                        H, Hkv, S, D, P, _layout(layout), int(bool(causal)),
                                        float(scale), _ptr(tiles), _stream(stream)))
     return out, lse, tiles
+
+
+def fwd_traced(q, k, v, P: int, layout, causal: bool = True, scale: float | None = None,
+               out_dtype=torch.bfloat16, stream=None):
+    """fwd plus the per-work-item timeline: (out, lse, records) with records a
+    CPU int64 tensor [items, 4] of (start ns, end ns, shard << 32 | CTA, key
+    tiles multiplied)."""
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = D ** -0.5
+    out = torch.empty((B, S, H, D), dtype=out_dtype, device=q.device)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    n = ctypes.c_int64(0)
+    L = lib()
+    # the number of items first (a call with no room fails before any launch)
+    L.ring_attn_fwd_traced(_ptr(q), _ptr(k), _ptr(v), _ptr(out), 0, _ptr(lse), B, H, Hkv, S, D,
+                           P, _layout(layout), int(bool(causal)), float(scale),
+                           ctypes.c_void_p(8), 0, ctypes.byref(n), _stream(stream))
+    rec = torch.empty((max(n.value, 1), 4), dtype=torch.int64, device=q.device)
+    odt = RA_F32 if out_dtype == torch.float32 else RA_BF16
+    _check(L.ring_attn_fwd_traced(_ptr(q), _ptr(k), _ptr(v), _ptr(out), odt, _ptr(lse), B, H,
+                                  Hkv, S, D, P, _layout(layout), int(bool(causal)), float(scale),
+                                  _ptr(rec), n.value, ctypes.byref(n), _stream(stream)))
+    return out, lse, rec[:n.value].cpu()
 
 
 def bwd(q, k, v, out, lse, dout, P: int, layout, causal: bool = True,

@@ -512,7 +512,7 @@ struct __align__(1024) DqSmem {
   uint8_t k[BwdCfg<D>::kStages][BwdCfg<D>::kTileBytes];
   uint8_t v[BwdCfg<D>::kStages][BwdCfg<D>::kTileBytes];
   uint64_t q_full, q_empty;
-  uint64_t qt_full;   // the unit's Q and dO are in tensor memory (256 arrivals)
+  uint64_t qt_full;   // the unit's Q and dO are in tensor memory (one arrival per warp)
   uint64_t st_full[BwdCfg<D>::kStages], st_empty[BwdCfg<D>::kStages];
   uint64_t s_full[2], p_full[2];
   uint64_t acc_full, acc_empty;
@@ -695,10 +695,10 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&sm.s_full[x]), 2);
-      mbar_init(smem_u32(&sm.p_full[x]), 128);
+      mbar_init(smem_u32(&sm.p_full[x]), 4);      // one arrival per elementwise warp
     }
     mbar_init(smem_u32(&sm.acc_full), 2);
-    mbar_init(smem_u32(&sm.acc_empty), 256);
+    mbar_init(smem_u32(&sm.acc_empty), 8);
     mbar_init(smem_u32(&sm.drain[0]), 1);
     mbar_init(smem_u32(&sm.drain[1]), 1);
     sm.abort_flag = 0;
@@ -914,7 +914,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           dkdv_half<false>(t_s, t_dp, nl, nd, sl2, lo, 64 * x);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&sm.p_full[x]));
+        mbar_arrive_warp(smem_u32(&sm.p_full[x]));
         if (++st == (uint32_t)kSt) { st = 0; st_ph ^= 1; }
         ++it.a;
       } while (qiter_next(g, it));
@@ -946,7 +946,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&sm.acc_empty));
+      mbar_arrive_warp(smem_u32(&sm.acc_empty));
     }
   }
 
@@ -993,18 +993,18 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
   if (tid == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
-    mbar_init(smem_u32(&sm.q_empty), 256);
-    mbar_init(smem_u32(&sm.qt_full), 256);
+    mbar_init(smem_u32(&sm.q_empty), 8);
+    mbar_init(smem_u32(&sm.qt_full), 8);
     for (int i = 0; i < kSt; ++i) {
       mbar_init(smem_u32(&sm.st_full[i]), 1);
       mbar_init(smem_u32(&sm.st_empty[i]), 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&sm.s_full[x]), 2);
-      mbar_init(smem_u32(&sm.p_full[x]), 128);
+      mbar_init(smem_u32(&sm.p_full[x]), 4);      // one arrival per elementwise warp
     }
     mbar_init(smem_u32(&sm.acc_full), 1);
-    mbar_init(smem_u32(&sm.acc_empty), 256);
+    mbar_init(smem_u32(&sm.acc_empty), 8);
     mbar_init(smem_u32(&sm.drain[0]), 1);
     mbar_init(smem_u32(&sm.drain[1]), 1);
     sm.abort_flag = 0;
@@ -1193,7 +1193,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&sm.acc_empty));
+      mbar_arrive_warp(smem_u32(&sm.acc_empty));
     };
     for (int64_t k = 0;; ++k) {
       const int64_t item = item_at(k);
@@ -1241,8 +1241,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tile_row_to_tmem<D>(a_src, row, t_a);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&sm.qt_full));
-      mbar_arrive(smem_u32(&sm.q_empty));
+      mbar_arrive_warp(smem_u32(&sm.qt_full));
+      mbar_arrive_warp(smem_u32(&sm.q_empty));
       if (owed) store_dq();
       do {
         const int k0 = it.bt * kTile;
@@ -1265,7 +1265,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           dq_half<false>(t_s, t_dp, sl2_2, nl2, nd2, lim, 64 * x);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&sm.p_full[x]));
+        mbar_arrive_warp(smem_u32(&sm.p_full[x]));
         ++it.bt;
       } while (kiterb_next(g, it));
       // ---- epilogue (deferred): half x stores dq columns [x*D/2, (x+1)*D/2), times scale

@@ -67,6 +67,10 @@ struct FwdParams {
   int out_f32;
   float* lse;          // may be null
   unsigned long long* shard_tiles;  // may be null: per-shard count of multiplied tile pairs
+  // may be null: per work item, 4 words: the globaltimer when its CTA took it
+  // up, when its last output row was stored (caller-zeroed, atomicMax), the
+  // shard << 32 | CTA, and the number of key tiles its query tiles multiplied
+  unsigned long long* trace;
   int64_t num_items;
   int kv_group;        // (b, kv head) pairs per scheduling group (see unit_head)
   // packed sequences (attn_fwd_kernel<D, true> only):
@@ -254,7 +258,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(smem_u32(&sm.q_full[x]), 1);
       mbar_init(smem_u32(&sm.q_empty[x]), 1);
       mbar_init(smem_u32(&sm.s_full[x]), 1);
-      mbar_init(smem_u32(&sm.p_full[x]), 128);
+      mbar_init(smem_u32(&sm.p_full[x]), 4);      // one arrival per softmax warp
       mbar_init(smem_u32(&sm.o_full[x]), 1);
     }
     for (int i = 0; i < Cfg::kKStages; ++i) {
@@ -313,6 +317,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const QTile qa = make_qtile(g, u.shard, u.seg, 2 * u.pair);
         const QTile qb = make_qtile(g, u.shard, u.seg, 2 * u.pair + 1);
         const int na = tile_work(g, qa, sblk), nb = tile_work(g, qb, sblk);
+        if (p.trace != nullptr) {
+          unsigned long long* rec = p.trace + 4 * item;
+          rec[0] = globaltimer();
+          rec[2] = (static_cast<unsigned long long>(u.shard) << 32) | blockIdx.x;
+          rec[3] = static_cast<unsigned long long>(na + nb);
+        }
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           const QTile& qt = x ? qb : qa;
@@ -637,7 +647,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           l_run += sum2.x + sum2.y;
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(smem_u32(&sm.p_full[x]));
+          mbar_arrive_warp(smem_u32(&sm.p_full[x]));
           ++it.bt;
         }
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_full[x]), o_ph,
@@ -691,6 +701,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (row_ok && p.lse != nullptr)
         p.lse[lidx] = has ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+      if (p.trace != nullptr) {
+        __syncwarp();
+        if (lane == 0) atomicMax(p.trace + 4 * item + 1, globaltimer());
+      }
     }
   }
 

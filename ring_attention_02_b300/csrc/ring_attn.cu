@@ -218,7 +218,8 @@ int fwd_kv_group(const ra::Geo& g, bool step, const DeviceInfo* dev, int D) {
 ra_status fwd_impl(int mode, const void* q, const void* k, const void* v, void* out, int out_f32,
                    float* lse, int B, int H, int Hkv, int64_t S, int D, int P, int layout,
                    int causal, float scale, int r, int s, unsigned long long* shard_tiles,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, unsigned long long* trace = nullptr,
+                   int64_t trace_capacity = 0) {
   if (!q || !k || !v || !out) return fail(RA_ERR_NULL, "q, k, v and out must be non-NULL");
   ra_status st = check_common(B, H, Hkv, S, D, P, layout, scale);
   if (st != RA_OK) return st;
@@ -244,6 +245,14 @@ ra_status fwd_impl(int mode, const void* q, const void* k, const void* v, void* 
   const bool step = mode == ra::FWD_MODE_STEP;
   prm.num_items = ra::units_total(prm.g, step) * B * H;
   prm.kv_group = fwd_kv_group(prm.g, step, dev, D);
+  if (trace != nullptr) {
+    if (trace_capacity < prm.num_items)
+      return fail(RA_ERR_SHAPE, "the trace holds %lld records; this call has %lld work items",
+                  (long long)trace_capacity, (long long)prm.num_items);
+    cudaError_t e = cudaMemsetAsync(trace, 0, (size_t)prm.num_items * 4 * sizeof(int64_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the trace");
+    prm.trace = trace;
+  }
 
   CUtensorMap mq, mk, mv;
   const int64_t n = S / P;
@@ -666,6 +675,24 @@ ra_status ring_attn_fwd_counted(const void* q, const void* k, const void* v, voi
                   layout, causal, scale, 0, 0,
                   reinterpret_cast<unsigned long long*>(shard_tiles),
                   static_cast<cudaStream_t>(stream));
+}
+
+ra_status ring_attn_fwd_traced(const void* q, const void* k, const void* v, void* out,
+                               ra_dtype out_dtype, float* lse, int B, int H, int Hkv, int64_t S,
+                               int D, int P, ra_layout layout, int causal, float scale,
+                               int64_t* records, int64_t capacity, int64_t* items, void* stream) {
+  if (out_dtype != RA_BF16 && out_dtype != RA_F32)
+    return fail(RA_ERR_UNSUPPORTED, "out_dtype %d", (int)out_dtype);
+  if (!records || !items) return fail(RA_ERR_NULL, "records and items must be non-NULL");
+  if (reinterpret_cast<uintptr_t>(records) & 7u)
+    return fail(RA_ERR_ALIGN, "records must be 8-byte aligned");
+  ra_status st = check_common(B, H, Hkv, S, D, P, (int)layout, scale);
+  if (st != RA_OK) return st;
+  *items = ra::units_total(ra::make_geo(B, H, Hkv, S, P, (int)layout, causal ? 1 : 0), false) *
+           B * H;
+  return fwd_impl(ra::FWD_MODE_RING, q, k, v, out, out_dtype == RA_F32, lse, B, H, Hkv, S, D, P,
+                  layout, causal, scale, 0, 0, nullptr, static_cast<cudaStream_t>(stream),
+                  reinterpret_cast<unsigned long long*>(records), capacity);
 }
 
 ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void* out,

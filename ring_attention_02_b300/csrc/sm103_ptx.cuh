@@ -60,6 +60,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// One arrival for the whole warp: the warp barrier orders every lane's earlier
+// work (tensor-memory stores already waited for and fenced with
+// tcgen05.fence::before_thread_sync, shared-memory reads and writes) before
+// lane 0's release-arrive.  A barrier a warpgroup signals this way counts 4
+// arrivals instead of 128: one arrive per thread serialises on the barrier
+// word for a few hundred cycles.  All 32 lanes must call it.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

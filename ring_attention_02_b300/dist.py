@@ -108,13 +108,41 @@ def _scale(D, scale):
     return D ** -0.5 if scale is None else float(scale)
 
 
+class HopTimeline:
+    """Per-hop timings of one rank's ring: for each step t the block s it
+    computed on, the device time of that hop's kernels and the time the rank
+    then spent waiting for the next block to arrive.  The pages' overlap
+    condition ("Zig Zag Ring Attention": compute per hop at least the transfer
+    per hop) holds where the waits stay near zero.  CUDA events on the current
+    stream; read the numbers with hops() after a synchronize."""
+
+    def __init__(self):
+        self._rec = []
+
+    def mark(self, t, s):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record()
+        self._rec.append((t, s, ev))
+        return ev
+
+    def hops(self):
+        out = []
+        for t, s, ev in self._rec:
+            out.append({"step": t, "block": s, "compute_ms": ev[0].elapsed_time(ev[1]),
+                        "wait_ms": ev[1].elapsed_time(ev[2])})
+        return out
+
+
 def ring_fwd(q, k, v, S: int, layout, causal: bool = True, scale: float | None = None,
-             comm: RingComm | None = None, out_dtype=torch.bfloat16):
+             comm: RingComm | None = None, out_dtype=torch.bfloat16,
+             timeline: HopTimeline | None = None):
     """Forward on rank r of a P-rank ring (P = the group size).
 
     q [B, n, H, D], k/v [B, n, Hkv, D]: this rank's shard r in local-slot order
     (bf16), n = S / P, shard contents fixed by `layout`.  Returns this shard's
     (out [B, n, H, D] in out_dtype (bf16 or fp32), lse [B, H, n] fp32).
+    With a HopTimeline (device tensors only), each hop's compute and wait
+    times are recorded in it.
     """
     comm = comm or RingComm()
     P, r = comm.world, comm.rank
@@ -134,15 +162,20 @@ def ring_fwd(q, k, v, S: int, layout, causal: bool = True, scale: float | None =
         if t < P - 1:
             nxt = bufs[t % 2]
             pend = comm.start(list(held), list(nxt))      # block s moves on while it is used
+        ev = timeline.mark(t, s) if timeline is not None else None
         if t == 0:
             api.step(q, held[0], held[1], S, P, layout, r, s, causal, scale, out=acc_o, lse=acc_l)
         else:
             api.step(q, held[0], held[1], S, P, layout, r, s, causal, scale, out=part_o,
                      lse=part_l)
             api.merge(acc_o, acc_l, part_o, part_l)
+        if ev is not None:
+            ev[1].record()
         if pend is not None:
             comm.finish(pend)
             held = nxt
+        if ev is not None:
+            ev[2].record()
     out = api.finalize(acc_o) if out_dtype == torch.bfloat16 else acc_o
     return out, acc_l
 

@@ -54,7 +54,13 @@ def _worker(rank, world, port, scheme, shape, layout, q):
         qs, ks, vs, dos = (shard(t) for t in (qf, kf, vf, dof))
         comm = rdist.RingComm()
         if scheme == "ring":
-            out, lse = rdist.ring_fwd(qs, ks, vs, S, layout, True, comm=comm)
+            tl = rdist.HopTimeline()
+            out, lse = rdist.ring_fwd(qs, ks, vs, S, layout, True, comm=comm, timeline=tl)
+            torch.cuda.synchronize()
+            hops = tl.hops()
+            assert [h["step"] for h in hops] == list(range(P))
+            assert [h["block"] for h in hops] == [(rank - t) % P for t in range(P)]
+            assert all(h["compute_ms"] > 0 and h["wait_ms"] >= 0 for h in hops)
             dq, dk, dv = rdist.ring_bwd(qs, ks, vs, out, lse, dos, S, layout, True, comm=comm)
         else:
             out, lse = rdist.ulysses_fwd(qs, ks, vs, S, layout, True, comm=comm)

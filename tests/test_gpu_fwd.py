@@ -255,3 +255,27 @@ def test_counted_tiles_match_oracle_census(layout, S, P):
     run = S // (2 * P) if layout == "zigzag" else 0
     _, ref = oracle.work_census(S, P, layout, True, tile=128, run=run)
     assert np.array_equal(tiles.cpu().numpy(), ref * B * H), (tiles.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+def test_traced_forward_timeline(layout):
+    # the per-work-item timeline: one record per item with end >= start, the
+    # key tiles multiplied per shard summing to the oracle's census, and the
+    # outputs bit-identical to the untraced forward
+    B, H, Hkv, S, D, P = 1, 4, 2, 8192, 128, 8
+    q, k, v = make_qkv(B, H, Hkv, S, D, seed=10, device="cuda")
+    out, lse, rec = api.fwd_traced(q, k, v, P, layout, True)
+    ref_o, ref_l = api.fwd(q, k, v, P, layout, True)
+    api.check_status()
+    assert torch.equal(out.view(torch.int16), ref_o.view(torch.int16))
+    assert torch.equal(lse, ref_l)
+    r = rec.numpy()
+    work = r[:, 3] > 0
+    assert np.all(r[work, 0] > 0) and np.all(r[work, 1] >= r[work, 0])
+    shard = (r[:, 2] >> 32).astype(np.int64)
+    per_shard = np.bincount(shard, weights=r[:, 3], minlength=P).astype(np.int64)
+    run = S // (2 * P) if layout == "zigzag" else 0
+    _, ref = oracle.work_census(S, P, layout, True, tile=128, run=run)
+    assert np.array_equal(per_shard, ref * B * H)
+    busy = np.bincount(shard, weights=(r[:, 1] - r[:, 0]) * work, minlength=P)
+    print(f"TIMELINE {layout}: per-shard busy ms {np.round(busy / 1e6, 3).tolist()}")
