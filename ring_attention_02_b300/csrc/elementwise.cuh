@@ -121,69 +121,86 @@ __global__ void cache_append_kernel(uint4* __restrict__ k_cache, uint4* __restri
 }
 
 // ---------------------------------------------------------------- merge
-// (out_acc, lse_acc) <- fold of (out_part, lse_part), rows (b, j, h):
+// (out_acc, lse_acc) <- fold of (out_part, lse_part) for rows (b, t, h):
 //   lse = max + ln(e^(l1 - max) + e^(l2 - max)),
 //   out = e^(l1 - lse) out_acc + e^(l2 - lse) out_part.
-// One row is handled by D/4 consecutive lanes of one warp (float4 each).  A
-// warp takes kMergeUnroll groups of rows per step and issues every load of the
-// step (both lse values and both float4 of each row) before it uses any, so a
-// step costs one memory round trip instead of two per row.  The row's lse is
-// read by all its lanes before lane 0 of the row writes it back (__syncwarp).
-// Idx is uint32_t when B * n * H fits, uint64_t otherwise.
+// A CTA takes a tile of kMergeTok consecutive tokens of one batch entry, all
+// H heads.  It first folds the tile's lse values, head by head: kMergeTok
+// consecutive floats of [B][H][n], one 32-byte sector per head, read and
+// written once by this CTA, with the two weights of each row kept in shared
+// memory.  Then it streams the tile's out rows, which are one contiguous run
+// of kMergeTok * H * D floats in [B][n][H][D], four float4 of each tensor in
+// flight per thread.  (A row-by-row order made every lse sector a read and a
+// write from eight different CTAs: 69 % of the measured HBM rate on the
+// 32-head shard against 90 % for this order.)
+constexpr int kMergeTok = 8;
+constexpr int kMergeThreads = 512;
 constexpr int kMergeUnroll = 4;
-constexpr int kMergeThreads = 256;
 
-template <int D, typename Idx>
+template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(float* __restrict__ out_acc, float* __restrict__ lse_acc,
-             const float* __restrict__ out_part, const float* __restrict__ lse_part, Idx H, Idx n,
-             Idx rows) {
-  constexpr int kLanesPerRow = D / 4;
-  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
-  constexpr int kRowsPerStep = kRowsPerWarp * kMergeUnroll;
-  const int lane = threadIdx.x % 32;
-  const int sub = lane / kLanesPerRow;        // which row of the warp's group
-  const int q4 = lane % kLanesPerRow;         // float4 index inside the row
-  const Idx warps_total = (Idx)gridDim.x * (kMergeThreads / 32);
-  const Idx warp0 = (Idx)blockIdx.x * (kMergeThreads / 32) + threadIdx.x / 32;
-  for (Idx base = warp0 * kRowsPerStep; base < rows; base += warps_total * kRowsPerStep) {
-    float l1[kMergeUnroll], l2[kMergeUnroll];
-    float4 oa[kMergeUnroll], op[kMergeUnroll];
-    Idx li[kMergeUnroll];
+             const float* __restrict__ out_part, const float* __restrict__ lse_part, int B, int H,
+             int n) {
+  extern __shared__ float merge_w[];         // [2][H * kMergeTok]: the rows' two weights
+  float* w1s = merge_w;
+  float* w2s = merge_w + H * kMergeTok;
+  constexpr int kQ = D / 4;                  // float4 per row
+  const int tiles_per_b = (n + kMergeTok - 1) / kMergeTok;
+  const int64_t tiles = (int64_t)B * tiles_per_b;
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int b = (int)(tile / tiles_per_b);
+    const int t0 = (int)(tile % tiles_per_b) * kMergeTok;
+    const int nt = n - t0 < kMergeTok ? n - t0 : kMergeTok;
+    for (int i = threadIdx.x; i < H * kMergeTok; i += kMergeThreads) {
+      const int h = i / kMergeTok, t = i % kMergeTok;
+      float w1 = 0.f, w2 = 0.f;
+      if (t < nt) {
+        const int64_t li = ((int64_t)b * H + h) * n + t0 + t;
+        const float l1 = lse_acc[li], l2 = __ldg(lse_part + li);
+        if (!(l1 == -INFINITY && l2 == -INFINITY)) {
+          const float mx = fmaxf(l1, l2);
+          const float lse = mx + logf(expf(l1 - mx) + expf(l2 - mx));
+          w1 = expf(l1 - lse);
+          w2 = expf(l2 - lse);
+          lse_acc[li] = lse;
+        }
+      }
+      w1s[i] = w1;
+      w2s[i] = w2;
+    }
+    __syncthreads();
+    const int64_t base = ((int64_t)b * n + t0) * H * kQ;
+    const int q4n = nt * H * kQ;
+    float4* oa = reinterpret_cast<float4*>(out_acc) + base;
+    const float4* op = reinterpret_cast<const float4*>(out_part) + base;
+    for (int j0 = threadIdx.x; j0 < q4n; j0 += kMergeThreads * kMergeUnroll) {
+      float4 a[kMergeUnroll], c[kMergeUnroll];
 #pragma unroll
-    for (int u = 0; u < kMergeUnroll; ++u) {
-      const Idx r = base + (Idx)(u * kRowsPerWarp + sub);   // row index in [B][n][H] order
-      l1[u] = -INFINITY;
-      l2[u] = -INFINITY;
-      li[u] = 0;
-      if (r < rows) {
-        const Idx h = r % H, t = r / H;
-        li[u] = (t / n * H + h) * n + t % n;
-        l1[u] = lse_acc[li[u]];
-        l2[u] = __ldg(lse_part + li[u]);
-        oa[u] = reinterpret_cast<const float4*>(out_acc + (uint64_t)r * D)[q4];
-        op[u] = __ldg(reinterpret_cast<const float4*>(out_part + (uint64_t)r * D) + q4);
+      for (int u = 0; u < kMergeUnroll; ++u) {
+        const int j = j0 + u * kMergeThreads;
+        if (j < q4n) {
+          a[u] = oa[j];
+          c[u] = __ldg(op + j);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeUnroll; ++u) {
+        const int j = j0 + u * kMergeThreads;
+        if (j < q4n) {
+          const int row = j / kQ;                 // t * H + h within the tile
+          const int wi = (row % H) * kMergeTok + row / H;
+          const float w1 = w1s[wi], w2 = w2s[wi];
+          float4 o;
+          o.x = w1 * a[u].x + w2 * c[u].x;
+          o.y = w1 * a[u].y + w2 * c[u].y;
+          o.z = w1 * a[u].z + w2 * c[u].z;
+          o.w = w1 * a[u].w + w2 * c[u].w;
+          oa[j] = o;
+        }
       }
     }
-    __syncwarp();
-#pragma unroll
-    for (int u = 0; u < kMergeUnroll; ++u) {
-      const Idx r = base + (Idx)(u * kRowsPerWarp + sub);
-      if (r >= rows) continue;
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      const bool empty = l1[u] == -INFINITY && l2[u] == -INFINITY;
-      if (!empty) {
-        const float mx = fmaxf(l1[u], l2[u]);
-        const float lse = mx + logf(expf(l1[u] - mx) + expf(l2[u] - mx));
-        const float w1 = expf(l1[u] - lse), w2 = expf(l2[u] - lse);
-        o.x = w1 * oa[u].x + w2 * op[u].x;
-        o.y = w1 * oa[u].y + w2 * op[u].y;
-        o.z = w1 * oa[u].z + w2 * op[u].z;
-        o.w = w1 * oa[u].w + w2 * op[u].w;
-        if (q4 == 0) lse_acc[li[u]] = lse;
-      }
-      reinterpret_cast<float4*>(out_acc + (uint64_t)r * D)[q4] = o;
-    }
+    __syncthreads();   // the weights are rewritten for the next tile
   }
 }
 

@@ -1014,40 +1014,33 @@ ra_status ring_attn_merge(float* out_acc, float* lse_acc, const float* out_part,
     return fail(RA_ERR_ALIGN, "out_acc and out_part must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(lse_acc) | reinterpret_cast<uintptr_t>(lse_part)) & 3u)
     return fail(RA_ERR_ALIGN, "lse pointers must be 4-byte aligned");
+  if (H > 2048) return fail(RA_ERR_UNSUPPORTED, "H=%d heads; the merge takes at most 2048", H);
+  if (n > 0x7fffffffLL) return fail(RA_ERR_SHAPE, "n=%lld exceeds 2^31-1", (long long)n);
   DeviceInfo* dev = nullptr;
   ra_status st = device_info(&dev);
   if (st != RA_OK) return st;
-  const int64_t rows = (int64_t)B * n * H;
-  const int64_t rows_per_block = (ra::kMergeThreads / 32) * (32 / (D / 4)) * ra::kMergeUnroll;
-  int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
-  // 32-bit indices when every row index and every stride sum stays below 2^32
-  const bool narrow = 2 * (rows + rows_per_block) < (int64_t(1) << 32);
-  const void* fn = D == 128 ? (narrow ? (const void*)ra::merge_kernel<128, uint32_t>
-                                      : (const void*)ra::merge_kernel<128, uint64_t>)
-                            : (narrow ? (const void*)ra::merge_kernel<64, uint32_t>
-                                      : (const void*)ra::merge_kernel<64, uint64_t>);
-  // one full wave of resident blocks; each warp then strides over the rows
-  int per_sm = 0;
-  cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, ra::kMergeThreads, 0);
-  if (oe != cudaSuccess) return cuda_fail(oe, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(merge)");
-  const int64_t cap = (int64_t)dev->sms * (per_sm > 0 ? per_sm : 1);
-  if (blocks > cap) blocks = cap;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (narrow) {
-    if (D == 128)
-      ra::merge_kernel<128, uint32_t><<<(unsigned)blocks, ra::kMergeThreads, 0, cs>>>(
-          out_acc, lse_acc, out_part, lse_part, (uint32_t)H, (uint32_t)n, (uint32_t)rows);
-    else
-      ra::merge_kernel<64, uint32_t><<<(unsigned)blocks, ra::kMergeThreads, 0, cs>>>(
-          out_acc, lse_acc, out_part, lse_part, (uint32_t)H, (uint32_t)n, (uint32_t)rows);
-  } else {
-    if (D == 128)
-      ra::merge_kernel<128, uint64_t><<<(unsigned)blocks, ra::kMergeThreads, 0, cs>>>(
-          out_acc, lse_acc, out_part, lse_part, (uint64_t)H, (uint64_t)n, (uint64_t)rows);
-    else
-      ra::merge_kernel<64, uint64_t><<<(unsigned)blocks, ra::kMergeThreads, 0, cs>>>(
-          out_acc, lse_acc, out_part, lse_part, (uint64_t)H, (uint64_t)n, (uint64_t)rows);
+  const size_t smem = 2 * (size_t)H * ra::kMergeTok * sizeof(float);
+  const void* fn = D == 128 ? (const void*)ra::merge_kernel<128> : (const void*)ra::merge_kernel<64>;
+  if (smem > 48 * 1024) {
+    cudaError_t ae = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem);
+    if (ae != cudaSuccess) return cuda_fail(ae, "cudaFuncSetAttribute(merge smem)");
   }
+  // one wave of resident blocks; each strides over the token tiles
+  int per_sm = 0;
+  cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, ra::kMergeThreads,
+                                                                 smem);
+  if (oe != cudaSuccess) return cuda_fail(oe, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(merge)");
+  const int64_t tiles = (int64_t)B * ((n + ra::kMergeTok - 1) / ra::kMergeTok);
+  const int64_t cap = (int64_t)dev->sms * (per_sm > 0 ? per_sm : 1);
+  const int64_t blocks = tiles < cap ? tiles : cap;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (D == 128)
+    ra::merge_kernel<128><<<(unsigned)blocks, ra::kMergeThreads, smem, cs>>>(
+        out_acc, lse_acc, out_part, lse_part, B, H, (int)n);
+  else
+    ra::merge_kernel<64><<<(unsigned)blocks, ra::kMergeThreads, smem, cs>>>(
+        out_acc, lse_acc, out_part, lse_part, B, H, (int)n);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "merge_kernel launch");
   return RA_OK;

@@ -279,3 +279,28 @@ def test_traced_forward_timeline(layout):
     assert np.array_equal(per_shard, ref * B * H)
     busy = np.bincount(shard, weights=(r[:, 1] - r[:, 0]) * work, minlength=P)
     print(f"TIMELINE {layout}: per-shard busy ms {np.round(busy / 1e6, 3).tolist()}")
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_permute_shards_and_head_split_bit_exact(layout):
+    # the all-to-all's blocks: shard-outer order equals the oracle's shard-major
+    # permutation with the shard axis moved out, and the head split is a plain
+    # transpose of [rows, parts, chunk]; both round-trip exactly
+    B, S, P, H, D = 2, 3072, 4, 8, 64
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x = torch.randn((B, S, H, D), device="cuda", generator=g).to(torch.bfloat16)
+    y = api.permute_shards(x, S, P, layout)
+    ref = oracle.permute(x.view(torch.int16).cpu().numpy(), S, P, layout)   # [B, S, H, D]
+    ref = ref.reshape(B, P, S // P, H, D).transpose(1, 0, 2, 3, 4)
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().reshape(ref.shape), ref)
+    back = api.permute_shards(y.view(P, B, S // P, H, D), S, P, layout, inverse=True,
+                              out=torch.empty_like(x))
+    assert torch.equal(back.view(torch.int16), x.view(torch.int16))
+    z = api.head_split(x, B * S, P)                                   # [P, B*S, H/P*D]
+    zr = x.view(torch.int16).cpu().numpy().reshape(B * S, P, H // P * D).transpose(1, 0, 2)
+    assert np.array_equal(z.view(torch.int16).cpu().numpy().reshape(zr.shape), zr)
+    zb = api.head_split(z, B * S, P, inverse=True)
+    assert torch.equal(zb.view(torch.int16), x.view(torch.int16))
+    acc = torch.randn((B, S, H, D), device="cuda", generator=g)
+    fin = api.finalize(acc)
+    assert torch.equal(fin.view(torch.int16), acc.to(torch.bfloat16).view(torch.int16))
