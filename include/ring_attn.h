@@ -380,6 +380,35 @@ ra_status ring_attn_census(int64_t S, int P, ra_layout layout, int causal,
                            int64_t* visible_pairs, int64_t* computed_tiles);
 
 /*
+ * ring_attn_work_schedule -- host side, no GPU involved: the list of work
+ * items each CTA of a persistent kernel of a ring-mode call of this shape
+ * takes, for a GPU of `sms` SMs and l2_bytes of L2.  kind 0: the forward
+ * (a work item is a pair of 128-row query tiles of one (b, head)); 1: the
+ * backward's dK/dV pass (one 128-key tile of one (b, kv head)); 2: its dQ pass
+ * (one 128-row query tile of one (b, head)).  The item list of each kernel is
+ * ordered so that CTAs running at the same time share tiles in L2, longest
+ * first within a group; the schedule hands the items out in that order, each
+ * to the CTA whose items so far sum to the least estimated work (tiles
+ * multiplied, plus a fixed cost per item), as a queue would when CTAs fall
+ * idle.  Work is the same whichever CTA takes an item, so the results do not
+ * depend on the schedule.  The calls that launch these kernels build it on
+ * the first call of a shape and keep it in device memory; ring_attn_bwd_noalloc
+ * does not use one.
+ *
+ * Layout (int32): offsets[G + 1] (G = the grid, min(items, sms)), then CTA 0's
+ * item ids in the order it takes them, CTA 1's, ...; CTA c's are the entries
+ * offsets[c] .. offsets[c+1]-1 after the offsets.  *n_out receives the number
+ * of ints, 0 when the call runs without a schedule (no more items than CTAs,
+ * or more than 2^22 items; each CTA c then takes item k*G + c in even rounds
+ * k and k*G + G-1-c in odd ones).  out == NULL only sizes it; otherwise
+ * capacity ints must hold it (RA_ERR_SHAPE if not).  Shape errors as
+ * ring_attn_fwd.
+ */
+ra_status ring_attn_work_schedule(int kind, int B, int H, int Hkv, int64_t S, int D, int P,
+                                  ra_layout layout, int causal, int sms, int64_t l2_bytes,
+                                  int* out, int64_t capacity, int64_t* n_out);
+
+/*
  * ring_attn_check_status -- waits for `stream`, then reports and clears the
  * device status word: RA_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded
  * wait since the last check, RA_ERR_CUDA if the stream holds an error, else RA_OK.

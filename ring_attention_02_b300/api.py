@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
             L.ring_attn_finalize.argtypes = [vp, vp, i64, vp]
             L.ring_attn_index_map.argtypes = [i64, i32, i32, vp]
             L.ring_attn_census.argtypes = [i64, i32, i32, i32, vp, vp]
+            L.ring_attn_work_schedule.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32, i32,
+                                                  i32, i64, vp, i64, vp]
             L.ring_attn_check_status.argtypes = [vp]
             L.ring_attn_wait_selfcheck.argtypes = [i32, vp, vp]
             L.ring_attn_set_wait_limit.argtypes = [i64]
@@ -401,6 +403,27 @@ def census(S: int, P: int, layout, causal: bool = True):
                                   ctypes.c_void_p(pairs.data_ptr()),
                                   ctypes.c_void_p(tiles.data_ptr())))
     return pairs, tiles
+
+
+SCHEDULE_KINDS = {"fwd": 0, "dkdv": 1, "dq": 2}
+
+
+def work_schedule(kind: str, B: int, H: int, Hkv: int, S: int, D: int, P: int, layout,
+                  causal: bool = True, sms: int = 148, l2_bytes: int = 126 * 1024 * 1024):
+    """Host-side: the per-CTA work-item lists the persistent forward ("fwd")
+    or backward pass ("dkdv", "dq") of a ring-mode call of this shape runs by,
+    as a list of G int lists (None when the call runs unscheduled)."""
+    n = ctypes.c_int64(0)
+    args = (SCHEDULE_KINDS[kind], B, H, Hkv, S, D, P, _layout(layout), int(bool(causal)), sms,
+            l2_bytes)
+    _check(lib().ring_attn_work_schedule(*args, None, 0, ctypes.byref(n)))
+    if n.value == 0:
+        return None
+    buf = (ctypes.c_int * n.value)()
+    _check(lib().ring_attn_work_schedule(*args, buf, n.value, ctypes.byref(n)))
+    flat = list(buf)
+    off, items = flat[:sms + 1], flat[sms + 1:]   # scheduled calls have more items than SMs
+    return [items[off[c]:off[c + 1]] for c in range(sms)]
 
 
 def check_status(stream=None):

@@ -76,6 +76,7 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int64_t num_items;
+  const int* sched;           // may be null: per-CTA item lists (see cta_items)
   // packed sequences (BWD_VARLEN only):
   const int4* units;          // (sequence, shard, segment, tile) per unit, longest first
   const int64_t* cu_seqlens;  // token offset of each sequence, and the total
@@ -228,7 +229,7 @@ struct KUnit {
   int64_t vbase;    // first element of this batch entry or sequence in the vectors
 };
 
-__device__ __forceinline__ KUnit kunit_of(const Geo& g, int64_t item) {
+__host__ __device__ __forceinline__ KUnit kunit_of(const Geo& g, int64_t item) {
   const int64_t U = (int64_t)g.P * g.nseg * g.ntile;
   const int64_t bg = item / U;
   const int64_t u = item % U;
@@ -259,7 +260,7 @@ struct QUnit {
   int64_t vbase;
 };
 
-__device__ __forceinline__ QUnit qunit_of(const Geo& g, int64_t item) {
+__host__ __device__ __forceinline__ QUnit qunit_of(const Geo& g, int64_t item) {
   const int64_t U = (int64_t)g.P * g.nseg * g.ntile;
   const int64_t bh = item / U;
   const int64_t u = item % U;
@@ -286,7 +287,7 @@ __device__ __forceinline__ QUnit qunit_of(const Geo& g, int64_t item) {
 // One hop: the key tiles of block step_s, resp. the query tiles of shard
 // step_r, per (b, kv head) or (b, head); keys in increasing and queries in
 // decreasing position.
-__device__ __forceinline__ KUnit kunit_step(const Geo& g, int s, int64_t item) {
+__host__ __device__ __forceinline__ KUnit kunit_step(const Geo& g, int s, int64_t item) {
   const int64_t U = (int64_t)g.nseg * g.ntile;
   const int64_t bg = item / U;
   const int64_t u = item % U;
@@ -299,7 +300,7 @@ __device__ __forceinline__ KUnit kunit_step(const Geo& g, int s, int64_t item) {
   return w;
 }
 
-__device__ __forceinline__ QUnit qunit_step(const Geo& g, int r, int64_t item) {
+__host__ __device__ __forceinline__ QUnit qunit_step(const Geo& g, int r, int64_t item) {
   const int64_t U = (int64_t)g.nseg * g.ntile;
   const int64_t bh = item / U;
   const int64_t u = item % U;
@@ -717,9 +718,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   // next streamed stage with its lap parity.  At function scope so that an
   // aborting CTA can wait for every load it issued.
   uint32_t tkv_ph = 0, tst = 0, tst_ph = 0;
-  const int64_t G = gridDim.x;
-  const int64_t c = blockIdx.x;
-  auto item_at = [&](int64_t k) -> int64_t { return k * G + ((k & 1) ? (G - 1 - c) : c); };
+  const CtaItems mine = cta_items(p.sched);
+  auto item_at = [&](int64_t k) -> int64_t { return cta_item(mine, k, p.num_items); };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1023,9 +1023,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   // streamed stage with its lap parity.  At function scope so that an
   // aborting CTA can wait for every load it issued.
   uint32_t tq_ph = 0, tst = 0, tst_ph = 0;
-  const int64_t G = gridDim.x;
-  const int64_t c = blockIdx.x;
-  auto item_at = [&](int64_t k) -> int64_t { return k * G + ((k & 1) ? (G - 1 - c) : c); };
+  const CtaItems mine = cta_items(p.sched);
+  auto item_at = [&](int64_t k) -> int64_t { return cta_item(mine, k, p.num_items); };
 
   if (warp == 0) {
     if (lane == 0) {

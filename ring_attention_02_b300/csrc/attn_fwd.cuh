@@ -73,6 +73,7 @@ struct FwdParams {
   unsigned long long* trace;
   int64_t num_items;
   int kv_group;        // (b, kv head) pairs per scheduling group (see unit_head)
+  const int* sched;    // may be null: per-CTA item lists (see cta_items)
   // packed sequences (attn_fwd_kernel<D, true> only):
   const int4* units;          // (sequence, shard, segment, pair) per unit, longest first
   const int64_t* cu_seqlens;  // token offset of each sequence in the pack, and the total
@@ -148,8 +149,9 @@ __device__ __forceinline__ const Geo& unit_head(const FwdParams& p, int64_t item
   }
 }
 
-__device__ __forceinline__ UnitHead unit_head_dense(const FwdParams& p, int64_t item) {
-  UnitHead u;
+// Item -> (unit, b * H + h) of the group-major order above (host and device).
+__host__ __device__ __forceinline__ int64_t unit_index_dense(const FwdParams& p, int64_t item,
+                                                            int* bh = nullptr) {
   const Geo& g = p.g;
   const int G = g.H / g.Hkv;
   const int BK = g.B * g.Hkv;
@@ -159,12 +161,22 @@ __device__ __forceinline__ UnitHead unit_head_dense(const FwdParams& p, int64_t 
   const int64_t rem = item % per_group;
   const int left = BK - grp * p.kv_group;
   const int hg = left < p.kv_group ? left : p.kv_group;   // pairs in this group
-  const int64_t unit = rem / ((int64_t)hg * G);
   const int r2 = (int)(rem % ((int64_t)hg * G));
-  const int bk = grp * p.kv_group + r2 / G;
-  u.b = bk / g.Hkv;
-  u.hkv = bk % g.Hkv;
-  u.h = u.hkv * G + r2 % G;
+  if (bh != nullptr) {
+    const int bk = grp * p.kv_group + r2 / G;
+    *bh = (bk / g.Hkv) * g.H + (bk % g.Hkv) * G + r2 % G;
+  }
+  return rem / ((int64_t)hg * G);
+}
+
+__device__ __forceinline__ UnitHead unit_head_dense(const FwdParams& p, int64_t item) {
+  UnitHead u;
+  const Geo& g = p.g;
+  int bh = 0;
+  const int64_t unit = unit_index_dense(p, item, &bh);
+  u.b = bh / g.H;
+  u.h = bh % g.H;
+  u.hkv = u.h / (g.H / g.Hkv);
   Unit w = unit_of(g, unit, p.mode == FWD_MODE_STEP, p.step_r);
   u.shard = w.shard;
   u.seg = w.seg;
@@ -292,11 +304,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint32_t q_ph0 = 0, q_ph1 = 0;
   uint32_t tk_st = 0, tk_ph = 0, tv_st = 0, tv_ph = 0;
 
-  // Static "snake" assignment of the longest-first item list: round k gives
-  // CTA c item k*G + c (k even) or k*G + G-1-c (k odd).
-  const int64_t G = gridDim.x;
-  const int64_t c = blockIdx.x;
-  auto item_at = [&](int64_t k) -> int64_t { return k * G + ((k & 1) ? (G - 1 - c) : c); };
+  // This CTA's work items, in the order every role takes them.
+  const CtaItems mine = cta_items(p.sched);
+  auto item_at = [&](int64_t k) -> int64_t { return cta_item(mine, k, p.num_items); };
 
   if (warp < 4) {
     // Producer / MMA / idle warps give registers to the two softmax warpgroups.

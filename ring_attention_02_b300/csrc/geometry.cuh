@@ -169,4 +169,35 @@ __host__ __device__ inline int tile_work(const Geo& g, const QTile& q, int step_
   return total;
 }
 
+// The work items CTA c of a G-CTA persistent grid takes, in order: its list in
+// a host-built schedule (int32 offsets[G + 1], then CTA 0's item ids, CTA 1's,
+// ...), or without one a snake over the item order (round k gives item
+// k*G + c for even k, k*G + G-1-c for odd k).
+struct CtaItems {
+  const int* list;
+  int64_t count, G, c;
+};
+
+#ifdef __CUDACC__
+__device__ __forceinline__ CtaItems cta_items(const int* sched) {
+  CtaItems w;
+  w.G = gridDim.x;
+  w.c = blockIdx.x;
+  w.list = nullptr;
+  w.count = 0;
+  if (sched != nullptr) {
+    const int a0 = __ldg(sched + w.c);
+    w.list = sched + w.G + 1 + a0;
+    w.count = __ldg(sched + w.c + 1) - a0;
+  }
+  return w;
+}
+
+// Item k of the CTA's sequence, or `none` past its end.
+__device__ __forceinline__ int64_t cta_item(const CtaItems& w, int64_t k, int64_t none) {
+  if (w.list != nullptr) return k < w.count ? (int64_t)__ldg(w.list + k) : none;
+  return k * w.G + ((k & 1) ? (w.G - 1 - w.c) : w.c);
+}
+#endif
+
 }  // namespace ra

@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "../../include/ring_attn.h"
@@ -151,6 +152,185 @@ ra_status make_token_map(CUtensorMap* m, const void* base, int D, int heads, int
   return RA_OK;
 }
 
+// ---------------------------------------------------------------- work schedules
+// A persistent kernel's work items come in a fixed order: grouped by (b, kv
+// head) so that the CTAs running at one time share key/value (or query) tiles
+// in L2, and longest first inside a group.  Without a schedule the kernels
+// deal that list out as a snake (round k: CTA c takes item k*G + c, or
+// k*G + G-1-c on odd rounds), which balances long against short only where a
+// group's items happen to line up with the rounds.  Here the list is dealt out
+// the way a queue would hand it to CTAs as they fall idle: each item, in
+// order, goes to the CTA whose items so far add up to the least estimated work
+// (the key or query tiles the item multiplies, plus a fixed cost per item).
+// Every CTA still takes its items in list order, so the L2 grouping holds.
+//
+// Layout in device memory (int32): offsets[G + 1], then the item ids of CTA 0,
+// CTA 1, ...; CTA c's are entries offsets[c] .. offsets[c+1]-1 after the
+// offsets.  A schedule depends only on the launch's shape, so each is built
+// once and kept for the life of the process (the kernels of a captured graph
+// may read it at any later replay).
+enum SchedKind { SCHED_FWD = 0, SCHED_DKDV = 1, SCHED_DQ = 2 };
+
+struct SchedKey {
+  int kind, dev, B, H, Hkv, P, layout, causal, mode, r, s, grid, kv_group;
+  int64_t S;
+  bool operator==(const SchedKey& o) const {
+    return kind == o.kind && dev == o.dev && B == o.B && H == o.H && Hkv == o.Hkv && P == o.P &&
+           layout == o.layout && causal == o.causal && mode == o.mode && r == o.r && s == o.s &&
+           grid == o.grid && kv_group == o.kv_group && S == o.S;
+  }
+};
+struct SchedEntry {
+  SchedKey key;
+  int* buf;
+};
+std::mutex g_sched_mu;
+std::vector<SchedEntry> g_scheds;
+constexpr size_t kSchedMax = 256;          // entries kept; later shapes run unscheduled
+constexpr int64_t kSchedItemsMax = 1 << 22;  // larger lists run unscheduled
+constexpr double kItemCost = 2.0;          // fixed cost of an item, in tile steps
+
+// Deals items 0..n-1 (estimated cost cost_of(unit_of(item)), units 0..U-1) to
+// G CTAs; returns offsets[G + 1] followed by the per-CTA item lists.
+template <class UnitOf>
+std::vector<int> deal_items(int64_t n, int G, const std::vector<double>& unit_cost, UnitOf unit_of) {
+  std::vector<std::vector<int>> lists((size_t)G);
+  typedef std::pair<double, int> Load;  // (work so far, CTA); ties go to the lower CTA
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> idle;
+  for (int c = 0; c < G; ++c) idle.push(Load(0.0, c));
+  for (int64_t i = 0; i < n; ++i) {
+    Load l = idle.top();
+    idle.pop();
+    lists[(size_t)l.second].push_back((int)i);
+    l.first += unit_cost[(size_t)unit_of(i)] + kItemCost;
+    idle.push(l);
+  }
+  std::vector<int> out;
+  out.reserve((size_t)(G + 1 + n));
+  int off = 0;
+  for (int c = 0; c < G; ++c) {
+    out.push_back(off);
+    off += (int)lists[(size_t)c].size();
+  }
+  out.push_back(off);
+  for (int c = 0; c < G; ++c) out.insert(out.end(), lists[(size_t)c].begin(), lists[(size_t)c].end());
+  return out;
+}
+
+// Query tiles (of shard r, or of every shard when r < 0) that see a key tile
+// whose first position is kmin: under a causal mask, those whose last position
+// is at or after kmin.  A segment's tiles past the one holding its first slot
+// at or after kmin all qualify.
+int64_t query_tiles_seeing(const ra::Geo& g, int kmin, int r) {
+  int64_t n = 0;
+  const int r0 = r < 0 ? 0 : r, r1 = r < 0 ? g.P : r + 1;
+  for (int sh = r0; sh < r1; ++sh)
+    for (int sg = 0; sg < g.nseg; ++sg) {
+      const ra::Seg q = ra::segment_of(g, sh, sg);
+      const int nt = (q.len + ra::kTile - 1) / ra::kTile;
+      if (!g.causal) { n += nt; continue; }
+      if (q.pos0 + q.stride * (q.len - 1) < kmin) continue;
+      const int o = kmin <= q.pos0 ? 0 : (kmin - q.pos0 + q.stride - 1) / q.stride;
+      n += nt - o / ra::kTile;
+    }
+  return n;
+}
+
+// The schedule for `key`, built on first use; nullptr (the kernels then use
+// the snake) when the list is short or very long, when the cache is full, or
+// when `stream` is being captured and the schedule does not exist yet.
+bool schedule_worth(int64_t n_items, int grid) {
+  return n_items > grid && n_items <= kSchedItemsMax;
+}
+
+template <class Build>
+const int* work_schedule(const SchedKey& key, int64_t n_items, cudaStream_t stream, Build build) {
+  if (!schedule_worth(n_items, key.grid)) return nullptr;
+  std::lock_guard<std::mutex> lk(g_sched_mu);
+  for (const SchedEntry& e : g_scheds)
+    if (e.key == key) return e.buf;
+  if (g_scheds.size() >= kSchedMax) return nullptr;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return nullptr;
+  const std::vector<int> host = build();
+  int* buf = nullptr;
+  if (cudaMalloc(&buf, host.size() * sizeof(int)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (cudaMemcpy(buf, host.data(), host.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cudaFree(buf);
+    return nullptr;
+  }
+  g_scheds.push_back(SchedEntry{key, buf});
+  return buf;
+}
+
+int current_device() {
+  int d = 0;
+  return cudaGetDevice(&d) == cudaSuccess ? d : -1;
+}
+
+// Forward (ring or step mode): a unit is a pair of query tiles; it multiplies
+// the union of the key tiles its two tiles see, i.e. those of its later tile.
+std::vector<int> fwd_schedule_host(const ra::FwdParams& prm, int grid) {
+  const ra::Geo& g = prm.g;
+  const bool step = prm.mode == ra::FWD_MODE_STEP;
+  const int64_t U = ra::units_total(g, step);
+  std::vector<double> cost((size_t)U);
+  for (int64_t u = 0; u < U; ++u) {
+    const ra::Unit w = ra::unit_of(g, u, step, prm.step_r);
+    ra::QTile q = ra::make_qtile(g, w.shard, w.seg, 2 * w.pair + 1);
+    if (!q.valid) q = ra::make_qtile(g, w.shard, w.seg, 2 * w.pair);
+    cost[(size_t)u] = ra::tile_work(g, q, step ? prm.step_s : -1);
+  }
+  return deal_items(prm.num_items, grid, cost,
+                    [&](int64_t item) { return ra::unit_index_dense(prm, item); });
+}
+
+const int* fwd_schedule(const ra::FwdParams& prm, int grid, cudaStream_t stream) {
+  const ra::Geo& g = prm.g;
+  SchedKey key{SCHED_FWD, current_device(), g.B, g.H, g.Hkv, g.P, g.layout, g.causal, prm.mode,
+               prm.step_r, prm.step_s, grid, prm.kv_group, (int64_t)g.S};
+  return work_schedule(key, prm.num_items, stream, [&]() { return fwd_schedule_host(prm, grid); });
+}
+
+// Backward (ring or hop mode): a dK/dV unit is one key tile of a (b, kv head)
+// and meets every query tile of the group's G heads that sees it; a dQ unit is
+// one query tile and meets the key tiles it sees.
+std::vector<int> bwd_schedule_host(const ra::BwdParams& prm, bool dkdv, bool step, int grid) {
+  const ra::Geo& g = prm.g;
+  const int64_t U = (int64_t)(step ? 1 : g.P) * g.nseg * g.ntile;
+  std::vector<double> cost((size_t)U);
+  const int G = g.H / g.Hkv;
+  for (int64_t u = 0; u < U; ++u) {
+    if (dkdv) {
+      const ra::KUnit w = step ? ra::kunit_step(g, prm.step_s, u) : ra::kunit_of(g, u);
+      const ra::Seg k = ra::segment_of(g, w.shard, w.seg);
+      const int kmin = k.pos0 + k.stride * (w.tile * ra::kTile);
+      cost[(size_t)u] = w.tile * ra::kTile < k.len
+                            ? (double)G * query_tiles_seeing(g, kmin, step ? prm.step_r : -1)
+                            : 0.0;
+    } else {
+      const ra::QUnit w = step ? ra::qunit_step(g, prm.step_r, u) : ra::qunit_of(g, u);
+      const ra::QTile q = ra::make_qtile(g, w.shard, w.seg, w.tile);
+      cost[(size_t)u] = ra::tile_work(g, q, step ? prm.step_s : -1);
+    }
+  }
+  return deal_items(prm.num_items, grid, cost, [&](int64_t item) { return item % U; });
+}
+
+const int* bwd_schedule(const ra::BwdParams& prm, bool dkdv, bool step, int grid,
+                        cudaStream_t stream) {
+  const ra::Geo& g = prm.g;
+  SchedKey key{dkdv ? SCHED_DKDV : SCHED_DQ, current_device(), g.B, g.H, g.Hkv, g.P, g.layout,
+               g.causal, step ? 1 : 0, prm.step_r, prm.step_s, grid, 0, (int64_t)g.S};
+  return work_schedule(key, prm.num_items, stream,
+                       [&]() { return bwd_schedule_host(prm, dkdv, step, grid); });
+}
+
 // ---------------------------------------------------------------- checks
 ra_status check_common(int B, int H, int Hkv, int64_t S, int D, int P, int layout, float scale) {
   if (B < 1 || H < 1 || Hkv < 1 || S < 1 || P < 1)
@@ -191,7 +371,9 @@ ra_status launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   }
   if (prm.num_items == 0) return RA_OK;
   const int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
-  ra::attn_fwd_kernel<D, kVarlen><<<(unsigned)grid, 384, smem, stream>>>(mq, mk, mv, prm);
+  ra::FwdParams run = prm;
+  if (!kVarlen) run.sched = fwd_schedule(prm, (int)grid, stream);
+  ra::attn_fwd_kernel<D, kVarlen><<<(unsigned)grid, 384, smem, stream>>>(mq, mk, mv, run);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel launch");
   return RA_OK;
@@ -316,7 +498,7 @@ ra_status bwd_attrs(DeviceInfo* dev) {
 
 template <int D>
 ra_status launch_bwd_d(const BwdArgs& a, float* nlse2, float* ndelta, DeviceInfo* dev,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, bool scheduled) {
   const size_t smem_kv = sizeof(ra::DkdvSmem<D>) + 1024;
   const size_t smem_q = sizeof(ra::DqSmem<D>) + 1024;
   {
@@ -361,12 +543,14 @@ ra_status launch_bwd_d(const BwdArgs& a, float* nlse2, float* ndelta, DeviceInfo
   const int64_t units = (int64_t)g.P * g.nseg * g.ntile;
   prm.num_items = units * a.B * a.Hkv;
   int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  prm.sched = scheduled ? bwd_schedule(prm, true, false, (int)grid, stream) : nullptr;
   ra::attn_bwd_dkdv_kernel<D, ra::BWD_RING><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dkdv_kernel launch");
 
   prm.num_items = units * a.B * a.H;
   grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  prm.sched = scheduled ? bwd_schedule(prm, false, false, (int)grid, stream) : nullptr;
   ra::attn_bwd_dq_kernel<D, ra::BWD_RING><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dq_kernel launch");
@@ -418,11 +602,13 @@ ra_status launch_bwd_step_d(const BwdArgs& a, int r, int s, int accumulate, floa
   const int64_t tiles = (int64_t)g.nseg * g.ntile;
   prm.num_items = tiles * a.B * a.Hkv;
   int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  prm.sched = bwd_schedule(prm, true, true, (int)grid, stream);
   ra::attn_bwd_dkdv_kernel<D, ra::BWD_STEP><<<(unsigned)grid, 384, smem_kv, stream>>>(mq, mk, mv, mdo, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dkdv_kernel launch");
   prm.num_items = tiles * a.B * a.H;
   grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
+  prm.sched = bwd_schedule(prm, false, true, (int)grid, stream);
   ra::attn_bwd_dq_kernel<D, ra::BWD_STEP><<<(unsigned)grid, 384, smem_q, stream>>>(mq, mk, mv, mdo, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_dq_kernel launch");
@@ -431,12 +617,15 @@ ra_status launch_bwd_step_d(const BwdArgs& a, int r, int s, int accumulate, floa
 
 // Launches the three backward kernels on `stream` with caller-provided
 // workspace: nlse2 and ndelta each hold vec_elems(geometry) floats.
-ra_status bwd_launch(const BwdArgs& a, float* nlse2, float* ndelta, cudaStream_t stream) {
+// `scheduled`: deal the work items by the cached host schedule (which is
+// allocated on first use of a shape) rather than the snake.
+ra_status bwd_launch(const BwdArgs& a, float* nlse2, float* ndelta, cudaStream_t stream,
+                     bool scheduled) {
   DeviceInfo* dev = nullptr;
   ra_status st = device_info(&dev);
   if (st != RA_OK) return st;
-  return a.D == 128 ? launch_bwd_d<128>(a, nlse2, ndelta, dev, stream)
-                    : launch_bwd_d<64>(a, nlse2, ndelta, dev, stream);
+  return a.D == 128 ? launch_bwd_d<128>(a, nlse2, ndelta, dev, stream, scheduled)
+                    : launch_bwd_d<64>(a, nlse2, ndelta, dev, stream, scheduled);
 }
 
 // ---------------------------------------------------------------- fixed backward workspace
@@ -717,7 +906,7 @@ ra_status ring_attn_bwd(const void* q, const void* k, const void* v, const void*
   }
   float* nlse2 = static_cast<float*>(ws);
   float* ndelta = reinterpret_cast<float*>(static_cast<char*>(ws) + vec_bytes);
-  st = bwd_launch(a, nlse2, ndelta, cs);
+  st = bwd_launch(a, nlse2, ndelta, cs, true);
   e = cudaFreeAsync(ws, cs);
   if (st != RA_OK) return st;
   if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(backward workspace)");
@@ -846,7 +1035,7 @@ ra_status ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, con
   float* ws = nullptr;
   st = fixed_workspace(static_cast<cudaStream_t>(stream), &ws);
   if (st != RA_OK) return st;
-  return bwd_launch(a, ws, ws + kFixedVecMax, static_cast<cudaStream_t>(stream));
+  return bwd_launch(a, ws, ws + kFixedVecMax, static_cast<cudaStream_t>(stream), false);
 }
 
 ra_status ring_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* out,
@@ -1210,6 +1399,48 @@ ra_status ring_attn_census(int64_t S, int P, ra_layout layout, int causal, int64
     if (visible_pairs) visible_pairs[r] = pairs;
     if (computed_tiles) computed_tiles[r] = tiles;
   }
+  return RA_OK;
+}
+
+ra_status ring_attn_work_schedule(int kind, int B, int H, int Hkv, int64_t S, int D, int P,
+                                  ra_layout layout, int causal, int sms, int64_t l2_bytes,
+                                  int* out, int64_t capacity, int64_t* n_out) {
+  if (n_out == nullptr) return fail(RA_ERR_NULL, "n_out must be non-NULL");
+  *n_out = 0;
+  if (kind < 0 || kind > 2)
+    return fail(RA_ERR_SHAPE, "kind %d: 0 (forward), 1 (dK/dV pass) or 2 (dQ pass)", kind);
+  if (sms < 1 || l2_bytes < 0 || l2_bytes > 0x7fffffffLL)
+    return fail(RA_ERR_SHAPE, "sms=%d and l2_bytes=%lld must be positive", sms, (long long)l2_bytes);
+  ra_status st = check_common(B, H, Hkv, S, D, P, (int)layout, 1.0f);
+  if (st != RA_OK) return st;
+  DeviceInfo dev;
+  dev.sms = sms;
+  dev.l2_bytes = (int)l2_bytes;
+  std::vector<int> v;
+  if (kind == 0) {
+    ra::FwdParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.g = ra::make_geo(B, H, Hkv, S, P, (int)layout, causal ? 1 : 0);
+    prm.mode = ra::FWD_MODE_RING;
+    prm.num_items = ra::units_total(prm.g, false) * B * H;
+    prm.kv_group = fwd_kv_group(prm.g, false, &dev, D);
+    const int grid = (int)(prm.num_items < sms ? prm.num_items : sms);
+    if (schedule_worth(prm.num_items, grid)) v = fwd_schedule_host(prm, grid);
+  } else {
+    ra::BwdParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.g = ra::make_geo(B, H, Hkv, S, P, (int)layout, causal ? 1 : 0);
+    const int64_t units = (int64_t)prm.g.P * prm.g.nseg * prm.g.ntile;
+    prm.num_items = units * B * (kind == 1 ? Hkv : H);
+    const int grid = (int)(prm.num_items < sms ? prm.num_items : sms);
+    if (schedule_worth(prm.num_items, grid)) v = bwd_schedule_host(prm, kind == 1, false, grid);
+  }
+  *n_out = (int64_t)v.size();
+  if (out == nullptr) return RA_OK;
+  if ((int64_t)v.size() > capacity)
+    return fail(RA_ERR_SHAPE, "the schedule holds %lld ints; the buffer %lld", (long long)v.size(),
+                (long long)capacity);
+  if (!v.empty()) memcpy(out, v.data(), v.size() * sizeof(int));
   return RA_OK;
 }
 
