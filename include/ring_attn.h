@@ -391,7 +391,8 @@ ra_status ring_attn_census(int64_t S, int P, ra_layout layout, int causal,
  * to the CTA whose items so far sum to the least estimated work (tiles
  * multiplied, plus a fixed cost per item), as a queue would when CTAs fall
  * idle.  Work is the same whichever CTA takes an item, so the results do not
- * depend on the schedule.  The calls that launch these kernels build it on
+ * depend on the schedule.  It is a scheduling policy of this library, with no
+ * counterpart on the pages.  The calls that launch these kernels build it on
  * the first call of a shape and keep it in device memory; ring_attn_bwd_noalloc
  * does not use one.
  *
