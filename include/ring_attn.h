@@ -393,8 +393,10 @@ ra_status ring_attn_census(int64_t S, int P, ra_layout layout, int causal,
  * idle.  Work is the same whichever CTA takes an item, so the results do not
  * depend on the schedule.  It is a scheduling policy of this library, with no
  * counterpart on the pages.  The calls that launch these kernels build it on
- * the first call of a shape and keep it in device memory; ring_attn_bwd_noalloc
- * does not use one.
+ * the first call of a shape (outside stream capture), copy it to device memory
+ * synchronously and keep it for the life of the process, up to 64 MiB of
+ * schedules in all; shapes past that, and ring_attn_bwd_noalloc, run without
+ * one.
  *
  * Layout (int32): offsets[G + 1] (G = the grid, min(items, sms)), then CTA 0's
  * item ids in the order it takes them, CTA 1's, ...; CTA c's are the entries

@@ -11,6 +11,7 @@
 #include <cstring>
 #include <mutex>
 #include <queue>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/ring_attn.h"
@@ -180,13 +181,27 @@ struct SchedKey {
            grid == o.grid && kv_group == o.kv_group && S == o.S;
   }
 };
-struct SchedEntry {
-  SchedKey key;
-  int* buf;
+struct SchedKeyHash {
+  size_t operator()(const SchedKey& k) const {
+    const int64_t f[] = {k.kind, k.dev,    k.B, k.H,    k.Hkv,  k.P,        k.layout,
+                         k.causal, k.mode, k.r, k.s, k.grid, k.kv_group, k.S};
+    uint64_t h = 1469598103934665603ull;  // FNV-1a over the fields
+    for (int64_t v : f) {
+      h ^= (uint64_t)v;
+      h *= 1099511628211ull;
+    }
+    return (size_t)h;
+  }
 };
 std::mutex g_sched_mu;
-std::vector<SchedEntry> g_scheds;
-constexpr size_t kSchedMax = 256;          // entries kept; later shapes run unscheduled
+// The kept schedules; nullptr for a shape refused for lack of budget (it then
+// runs unscheduled without being built again).
+std::unordered_map<SchedKey, int*, SchedKeyHash> g_scheds;
+// Device memory the kept schedules may take (a hop of a ring keys its own
+// schedule by (r, s), so a P-rank ring keeps up to P^2 small ones); shapes
+// past the budget run unscheduled.
+constexpr size_t kSchedBytesMax = (size_t)64 << 20;
+size_t g_sched_bytes = 0;
 constexpr int64_t kSchedItemsMax = 1 << 22;  // larger lists run unscheduled
 constexpr double kItemCost = 2.0;          // fixed cost of an item, in tile steps
 
@@ -237,8 +252,9 @@ int64_t query_tiles_seeing(const ra::Geo& g, int kmin, int r) {
 }
 
 // The schedule for `key`, built on first use; nullptr (the kernels then use
-// the snake) when the list is short or very long, when the cache is full, or
-// when `stream` is being captured and the schedule does not exist yet.
+// the snake) when the list is short or very long, when the schedules kept
+// would exceed their memory budget, or when `stream` is being captured and the
+// schedule does not exist yet.
 bool schedule_worth(int64_t n_items, int grid) {
   return n_items > grid && n_items <= kSchedItemsMax;
 }
@@ -247,12 +263,17 @@ template <class Build>
 const int* work_schedule(const SchedKey& key, int64_t n_items, cudaStream_t stream, Build build) {
   if (!schedule_worth(n_items, key.grid)) return nullptr;
   std::lock_guard<std::mutex> lk(g_sched_mu);
-  for (const SchedEntry& e : g_scheds)
-    if (e.key == key) return e.buf;
-  if (g_scheds.size() >= kSchedMax) return nullptr;
+  const auto hit = g_scheds.find(key);
+  if (hit != g_scheds.end()) return hit->second;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
     return nullptr;
+  // the list holds G + 1 offsets and n_items ids
+  const size_t bytes = ((size_t)key.grid + 1 + (size_t)n_items) * sizeof(int);
+  if (g_sched_bytes + bytes > kSchedBytesMax) {
+    g_scheds.emplace(key, nullptr);
+    return nullptr;
+  }
   const std::vector<int> host = build();
   int* buf = nullptr;
   if (cudaMalloc(&buf, host.size() * sizeof(int)) != cudaSuccess) {
@@ -264,7 +285,8 @@ const int* work_schedule(const SchedKey& key, int64_t n_items, cudaStream_t stre
     cudaFree(buf);
     return nullptr;
   }
-  g_scheds.push_back(SchedEntry{key, buf});
+  g_scheds.emplace(key, buf);
+  g_sched_bytes += host.size() * sizeof(int);
   return buf;
 }
 
