@@ -371,6 +371,67 @@ def measure_e2e(w, api, make_step, dev_in, dev_out, dev_scratch, dev, flops, wor
             "pipelined": "double-buffered; H2D, compute and D2H on separate streams"}
 
 
+def other_configs(api, dev, seed: int) -> dict:
+    """The other problem configurations, timed on the device after the headline's
+    timed region (default single-GPU run only): CUDA events on the launching
+    stream around `steps` calls after `warmup`, inputs resident, clocks sampled."""
+    from ring_attention_02_b300.inputs import TINY, CAUSAL_8K, GQA_128K, MILLION, TRAIN_32K
+    peak, _, _ = measured_peaks()
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for w, steps, warmup in ((TINY, 200, 5), (CAUSAL_8K, 20, 3), (GQA_128K, 3, 3),
+                             (MILLION, 2, 3), (TRAIN_32K, 3, 3)):
+        q, k, v = make_for(w, seed=seed, device=dev)
+        o = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.float32 if w.out_f32 else torch.bfloat16,
+                        device=dev)
+        lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+        if w.backward:
+            do = make_dout(w.B, w.H, w.S, w.D, seed=seed, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+
+        def step(i=None):
+            if i is not None:
+                ev[i][0].record(stream)
+            api.fwd(q, k, v, w.P, w.layout, w.causal, out=o, lse=lse, stream=stream)
+            if i is not None:
+                ev[i][1].record(stream)
+            if w.backward:
+                api.bwd(q, k, v, o, lse, do, w.P, w.layout, w.causal, dq=dq, dk=dk, dv=dv,
+                        stream=stream)
+                if i is not None:
+                    ev[i][2].record(stream)
+
+        for _ in range(warmup):
+            step()
+        api.check_status(stream)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev.index or 0) as clk:
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for i in range(steps):
+                step(i)
+            t1.record(stream)
+            torch.cuda.synchronize(dev)
+        api.check_status(stream)
+        ms = t0.elapsed_time(t1) / steps
+        value = w.step_flops() / (ms * 1e-3) / 1e12
+        rec = {"layout": w.layout, "causal": w.causal, "steps": steps, "warmup": warmup,
+               "ms_per_step": ms, "value": value, "unit": UNIT, "frac": value / peak,
+               "clocks": clk.summary()}
+        if w.backward:
+            f_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+            b_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+            b_tf = 2.5 * w.counted_flops() / (b_ms * 1e-3) / 1e12
+            rec.update({"fwd_ms": f_ms, "bwd_ms": b_ms, "bwd_value": b_tf, "bwd_frac": b_tf / peak})
+        out[w.name] = rec
+        del q, k, v, o, lse
+        if w.backward:
+            del do, dq, dk, dv
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w: Workload, rank: int, world: int):
     from ring_attention_02_b300 import api
 
@@ -505,6 +566,11 @@ def run_ours(args, w: Workload, rank: int, world: int):
     if w.backward:
         line["fwd_ms"] = sum(fwd_ms) / len(fwd_ms)
         line["bwd_ms"] = sum(bwd_ms) / len(bwd_ms)
+    if world == 1 and w.name == HEADLINE.name and not args.headline_only:
+        # outside the headline's timed region; the headline's value does not include them
+        del q, k, v, out, lse
+        torch.cuda.empty_cache()
+        line["other_configs"] = other_configs(api, dev, args.seed)
     print(json.dumps(line), flush=True)
 
 
@@ -742,6 +808,8 @@ def main(argv=None):
     ap.add_argument("--ref-prefix", type=int, default=12288,
                     help="training workloads: tokens of the oracle's fwd+bwd sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other configurations the default single-GPU run adds")
     ap.add_argument("--decode-tokens", type=int, default=1, help="--op decode: new tokens T")
     ap.add_argument("--sp-ranks", type=int, default=0,
                     help="--op sp_rank: ranks of the two schemes (default min(P, Hkv))")
