@@ -391,12 +391,12 @@ def other_configs(api, dev, seed: int) -> dict:
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
 
         def step(i=None):
-            if i is not None:
+            if i is not None and w.backward:
                 ev[i][0].record(stream)
             api.fwd(q, k, v, w.P, w.layout, w.causal, out=o, lse=lse, stream=stream)
-            if i is not None:
-                ev[i][1].record(stream)
             if w.backward:
+                if i is not None:
+                    ev[i][1].record(stream)
                 api.bwd(q, k, v, o, lse, do, w.P, w.layout, w.causal, dq=dq, dk=dk, dv=dv,
                         stream=stream)
                 if i is not None:
@@ -446,16 +446,19 @@ def run_ours(args, w: Workload, rank: int, world: int):
         do = make_dout(w.B, w.H, w.S, w.D, seed=args.seed + 17 * rank, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
-    # events: [fwd start, fwd end (= bwd start), bwd end] per timed step
+    # events: [fwd start, fwd end (= bwd start), bwd end] per timed step of a
+    # training workload; a forward-only step is its one launch, timed by the
+    # events around the whole region (per-step event records would add host
+    # work between the calls of a short one)
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
 
     def step(i=None):
-        if i is not None:
+        if i is not None and w.backward:
             marks[i][0].record(stream)
         api.fwd(q, k, v, w.P, w.layout, w.causal, out=out, lse=lse, stream=stream)
-        if i is not None:
-            marks[i][1].record(stream)
         if w.backward:
+            if i is not None:
+                marks[i][1].record(stream)
             api.bwd(q, k, v, out, lse, do, w.P, w.layout, w.causal, dq=dq, dk=dk, dv=dv,
                     stream=stream)
             if i is not None:
@@ -482,7 +485,7 @@ def run_ours(args, w: Workload, rank: int, world: int):
     ms_per_step = total_ms / args.steps
     flops = w.step_flops()
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
-    fwd_ms = [m[0].elapsed_time(m[1]) for m in marks]
+    fwd_ms = [m[0].elapsed_time(m[1]) for m in marks] if w.backward else [ms_per_step]
     bwd_ms = [m[1].elapsed_time(m[2]) for m in marks] if w.backward else []
 
     # ---- end to end through host buffers (pinned), C-ABI calls per step

@@ -74,6 +74,7 @@ struct FwdParams {
   int64_t num_items;
   int kv_group;        // (b, kv head) pairs per scheduling group (see unit_head)
   const int* sched;    // may be null: per-CTA item lists (see cta_items)
+  int early;           // launched with programmatic stream serialization
   // packed sequences (attn_fwd_kernel<D, true> only):
   const int4* units;          // (sequence, shard, segment, pair) per unit, longest first
   const int64_t* cu_seqlens;  // token offset of each sequence in the pack, and the total
@@ -295,6 +296,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Everything above touched only this CTA's shared and tensor memory; from
+  // here on the kernel reads and writes global memory.
+  if (p.early) {
+    griddep_launch_dependents();
+    griddep_wait();
+  }
   const uint32_t tmem = sm.tmem_base;
   const int sblk = step_block(p);
 

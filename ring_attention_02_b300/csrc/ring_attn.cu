@@ -395,7 +395,26 @@ ra_status launch_fwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
   const int64_t grid = prm.num_items < dev->sms ? prm.num_items : dev->sms;
   ra::FwdParams run = prm;
   if (!kVarlen) run.sched = fwd_schedule(prm, (int)grid, stream);
-  ra::attn_fwd_kernel<D, kVarlen><<<(unsigned)grid, 384, smem, stream>>>(mq, mk, mv, run);
+  // Programmatic stream serialization for a launch of fewer CTAs than SMs:
+  // it may begin while the kernel before it in the stream finishes (its CTAs
+  // land on SMs that are free and wait in griddep_wait() before touching
+  // global memory), so back-to-back small calls overlap one kernel's start
+  // with the previous one's end.  A full-width launch gains nothing from it
+  // and measured slower with it.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(384);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  // (a traced call follows its own memset: never early)
+  run.early = prm.trace == nullptr && grid < dev->sms ? 1 : 0;
+  cfg.numAttrs = run.early ? 1 : 0;
+  cudaError_t le = cudaLaunchKernelEx(&cfg, ra::attn_fwd_kernel<D, kVarlen>, mq, mk, mv, run);
+  if (le != cudaSuccess) return cuda_fail(le, "attn_fwd_kernel launch");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel launch");
   return RA_OK;

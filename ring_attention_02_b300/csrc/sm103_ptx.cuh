@@ -116,6 +116,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   }
 }
 
+// ---------------------------------------------------------------- dependent launch
+// A kernel launched with programmatic stream serialization may start while the
+// kernel before it in the stream is still running.  griddep_wait() blocks until
+// every prerequisite grid has completed and its memory is visible: call it
+// before the first access to global memory.  griddep_launch_dependents() lets
+// the next such kernel in the stream be scheduled before this one ends (its
+// CTAs still wait in griddep_wait() for this one to complete).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
