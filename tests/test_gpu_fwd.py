@@ -304,3 +304,34 @@ def test_permute_shards_and_head_split_bit_exact(layout):
     acc = torch.randn((B, S, H, D), device="cuda", generator=g)
     fin = api.finalize(acc)
     assert torch.equal(fin.view(torch.int16), acc.to(torch.bfloat16).view(torch.int16))
+
+
+@pytest.mark.parametrize("side_stream", [False, True])
+def test_back_to_back_small_calls_see_the_writes_before_them(side_stream):
+    # A forward of fewer work items than SMs may start while the kernel before it
+    # in the stream finishes; it must still read the inputs that kernel wrote and
+    # leave its own outputs last.  Each call's q is rewritten in place by a torch
+    # kernel just before it, into the same buffer, and every call writes the same
+    # out / lse buffers; each result is checked against the oracle.
+    B, H, Hkv, S, D, P = 1, 2, 2, 256, 64, 4
+    q0, k, v = make_qkv(B, H, Hkv, S, D, seed=41, device="cuda")
+    qbuf = torch.empty_like(q0)
+    out = torch.empty((B, S, H, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream() if side_stream else torch.cuda.current_stream()
+    factors = [0.25 * (i + 1) for i in range(12)]
+    outs, lses = [], []
+    with torch.cuda.stream(stream):
+        for f in factors:
+            qbuf.copy_(q0 * f)
+            api.fwd(qbuf, k, v, P, "contiguous", False, out=out, lse=lse, stream=stream)
+            outs.append(out.clone())
+            lses.append(lse.clone())
+    torch.cuda.synchronize()
+    api.check_status()
+    k64, v64 = to64(k), to64(v)
+    for f, o, l in zip(factors, outs, lses):
+        qf = (q0 * f).to(torch.bfloat16)
+        ro, rl = oracle.attn_fwd(to64(qf), k64, v64, False, D ** -0.5)
+        eo, el = max_abs(to64(o), ro), max_abs(to64(l), rl)
+        assert eo <= OUT_TOL and el <= LSE_TOL, (f, eo, el)
