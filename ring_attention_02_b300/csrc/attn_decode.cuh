@@ -100,6 +100,9 @@ decode_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const Geo& g = p.g;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  // the combine kernel that follows may be scheduled now: it waits for this
+  // grid to complete before reading the partials
+  griddep_launch_dependents();
   const int G = g.H / g.Hkv;
   const int bk = blockIdx.y;
   const int b = bk / g.Hkv, hkv = bk % g.Hkv;
@@ -344,6 +347,9 @@ decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict_
                       void* out, int out_f32, float* lse, Geo g, int T, int rows, int chunks) {
   constexpr int kPer = D / 32;
   __shared__ float red[kCombineWarps][D + 2];
+  // launched to overlap the partial kernel's end: its partials are complete
+  // and visible only after this
+  griddep_wait();
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   const int item = blockIdx.x;                 // (bk, i)
   const int i = item % rows, bk = item / rows;

@@ -734,9 +734,21 @@ ra_status launch_decode_d(const CUtensorMap& mk, const CUtensorMap& mv, const ra
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "decode_partial_kernel launch");
   const int64_t items = (int64_t)g.B * g.Hkv * prm.rows;
-  ra::decode_combine_kernel<D><<<(unsigned)items, ra::kCombineWarps * 32, 0, stream>>>(
-      prm.part_o, prm.part_lse, out, out_f32, lse, g, prm.T, prm.rows, prm.chunks);
-  e = cudaGetLastError();
+  // programmatic stream serialization: the combine is scheduled while the
+  // partial kernel's last CTAs run and waits (griddep_wait) for its partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)items);
+  cfg.blockDim = dim3(ra::kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, ra::decode_combine_kernel<D>, (const float*)prm.part_o,
+                         (const float*)prm.part_lse, out, out_f32, lse, g, prm.T, prm.rows,
+                         prm.chunks);
   if (e != cudaSuccess) return cuda_fail(e, "decode_combine_kernel launch");
   return RA_OK;
 }
