@@ -183,9 +183,9 @@ struct SchedKey {
 };
 struct SchedKeyHash {
   size_t operator()(const SchedKey& k) const {
-    const int64_t f[] = {k.kind, k.dev,    k.B, k.H,    k.Hkv,  k.P,        k.layout,
+    const int64_t f[] = {k.kind,   k.dev,  k.B, k.H, k.Hkv,  k.P,        k.layout,
                          k.causal, k.mode, k.r, k.s, k.grid, k.kv_group, k.S};
-    uint64_t h = 1469598103934665603ull;  // FNV-1a over the fields
+    uint64_t h = 1469598103934665603ull;  // FNV-style: xor in a field, multiply
     for (int64_t v : f) {
       h ^= (uint64_t)v;
       h *= 1099511628211ull;
