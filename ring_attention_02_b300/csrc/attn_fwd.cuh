@@ -52,8 +52,8 @@ enum { FWD_MODE_RING = 0, FWD_MODE_STEP = 1 };
 // control warpgroup drops to kRegsControl and the two softmax warpgroups rise
 // to kRegsSoftmax, using exactly the launched total.
 constexpr int kRegsLaunch = 168;
-constexpr uint32_t kRegsControl = 88;
-constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsControl = 72;
+constexpr uint32_t kRegsSoftmax = 216;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * kRegsLaunch,
               "register split exceeds the launch budget");
 
